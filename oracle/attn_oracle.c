@@ -1,0 +1,196 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg use it.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes is the plain definition, with no tiling, fusion or online
+ * rescaling:
+ *
+ *   s_ij  = scale * sum_d q_id k_jd                 (for j in the allowed set A_i)
+ *   LSE_i = m_i + ln sum_{j in A_i} exp(s_ij - m_i),   m_i = max_j s_ij
+ *   P_ij  = exp(s_ij - LSE_i)
+ *   O_i   = sum_j P_ij v_j
+ *
+ * with A_i = {0..N-1}, or {0..i} when causal.  Sources:
+ *   - exact attention O = softmax(scale QK^T) V, never materialising N x N:
+ *     FlashNystrom page, "Scope"; FlashStieltjes page, "The kernel";
+ *     "From-scratch CUDA attention kernel reaches 94.4% of FlashAttention-4",
+ *     "How the kernel partitions its work".
+ *   - the running-max / running-sum softmax reaches exactly this result:
+ *     FlashStieltjes page, "The challenge".
+ *   - causal keys j <= i, grouped-query heads (Hq a multiple of Hkv), ragged N:
+ *     FlashAttention for Tesla P100 page, "What it supports" and "Quick start"
+ *     (q is (B,Hq,N,D), k and v are (B,Hkv,N,D)).
+ *   - backward dS = P o (dP - Delta), Delta_i = dO_i . O_i, dV = P^T dO:
+ *     FlashAttention for Tesla P100 page, "Documentation".
+ *
+ * Readings where the pages are silent (stated once here, tested in tests/):
+ *   - query head h uses key/value head h / (Hq/Hkv) (consecutive groups);
+ *   - causal means key j <= query i (Nq == Nk, so both alignments agree);
+ *   - LSE is the natural log of the scaled scores;
+ *   - the backward's Delta uses the oracle's own fp64 O.
+ *
+ * All inputs are fp64 arrays (the caller widens bf16 exactly).  Layouts are
+ * contiguous [B, H, N, D] row-major; lse is [B, Hq, N].  OpenMP parallelises
+ * over independent rows (forward) and over (batch, kv-head) groups (backward).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Index of element (b, h, n, d) in a contiguous [B, H, N, D] tensor. */
+static inline int64_t at4(int64_t b, int64_t h, int64_t n, int64_t d,
+                          int64_t H, int64_t N, int64_t D) {
+  return ((b * H + h) * N + n) * D + d;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Scores of one query row against its allowed keys; returns |A_i|. */
+static int64_t row_scores(const double* qi, const double* kh, int64_t N, int64_t D,
+                          int64_t i, int causal, double scale, double* s) {
+  int64_t nallowed = causal ? (i + 1 < N ? i + 1 : N) : N;
+  for (int64_t j = 0; j < nallowed; ++j) {
+    const double* kj = kh + j * D;
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += qi[d] * kj[d];
+    s[j] = scale * dot;
+  }
+  return nallowed;
+}
+
+/* Softmax of a score row into probabilities; returns LSE (natural log). */
+static double row_softmax(double* s, int64_t n) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) if (s[j] > m) m = s[j];
+  double sum = 0.0;
+  for (int64_t j = 0; j < n; ++j) sum += exp(s[j] - m);
+  double lse = m + log(sum);
+  for (int64_t j = 0; j < n; ++j) s[j] = exp(s[j] - lse);
+  return lse;
+}
+
+/*
+ * Forward on a list of rows.  rows[r] is the flat row id (b*Hq + h)*N + i;
+ * rows == NULL means every row in order.  o is [nrows, D], lse is [nrows].
+ * Returns 0, or -1 on bad sizes / allocation failure.
+ */
+int oracle_fwd_rows(const double* q, const double* k, const double* v,
+                    int B, int Hq, int Hkv, int N, int D, int causal, double scale,
+                    const int64_t* rows, int64_t nrows, double* o, double* lse) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || D <= 0 || Hq % Hkv) return -1;
+  const int64_t G = Hq / Hkv;
+  const int64_t total = (int64_t)B * Hq * N;
+  if (!rows) nrows = total;
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+    if (!s) {
+#pragma omp atomic write
+      err = -1;
+    }
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t r = 0; r < nrows; ++r) {
+      if (!s) continue;
+      int64_t id = rows ? rows[r] : r;
+      if (id < 0 || id >= total) {
+#pragma omp atomic write
+        err = -1;
+        continue;
+      }
+      int64_t i = id % N, bh = id / N, h = bh % Hq, b = bh / Hq, hk = h / G;
+      const double* qi = q + at4(b, h, i, 0, Hq, N, D);
+      const double* kh = k + at4(b, hk, 0, 0, Hkv, N, D);
+      const double* vh = v + at4(b, hk, 0, 0, Hkv, N, D);
+      int64_t n = row_scores(qi, kh, N, D, i, causal, scale, s);
+      lse[r] = row_softmax(s, n);
+      double* oi = o + r * (int64_t)D;
+      for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+      for (int64_t j = 0; j < n; ++j) {
+        const double* vj = vh + j * D;
+        for (int64_t d = 0; d < D; ++d) oi[d] += s[j] * vj[d];
+      }
+    }
+    free(s);
+  }
+  return err;
+}
+
+/*
+ * Backward: given dO, returns dQ [B,Hq,N,D], dK and dV [B,Hkv,N,D].
+ *   Delta_i = sum_d dO_id O_id,  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - Delta_i)
+ *   dQ_i = scale sum_j dS_ij k_j
+ *   dK_j = scale sum_{h in group} sum_i dS_ij q_i
+ *   dV_j = sum_{h in group} sum_i P_ij dO_i
+ * One OpenMP task per (b, kv-head) so dK/dV have a single writer.
+ */
+int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
+               int B, int Hq, int Hkv, int N, int D, int causal, double scale,
+               double* dq, double* dk, double* dv) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || D <= 0 || Hq % Hkv) return -1;
+  const int64_t G = Hq / Hkv;
+  memset(dq, 0, sizeof(double) * (size_t)B * Hq * N * D);
+  memset(dk, 0, sizeof(double) * (size_t)B * Hkv * N * D);
+  memset(dv, 0, sizeof(double) * (size_t)B * Hkv * N * D);
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+    double* oi = (double*)malloc(sizeof(double) * D);
+    if (!s || !oi) {
+#pragma omp atomic write
+      err = -1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t g = 0; g < (int64_t)B * Hkv; ++g) {
+      if (!s || !oi) continue;
+      int64_t b = g / Hkv, hk = g % Hkv;
+      const double* kh = k + at4(b, hk, 0, 0, Hkv, N, D);
+      const double* vh = v + at4(b, hk, 0, 0, Hkv, N, D);
+      double* dkh = dk + at4(b, hk, 0, 0, Hkv, N, D);
+      double* dvh = dv + at4(b, hk, 0, 0, Hkv, N, D);
+      for (int64_t h = hk * G; h < (hk + 1) * G; ++h) {
+        for (int64_t i = 0; i < N; ++i) {
+          const double* qi = q + at4(b, h, i, 0, Hq, N, D);
+          const double* doi = dout + at4(b, h, i, 0, Hq, N, D);
+          double* dqi = dq + at4(b, h, i, 0, Hq, N, D);
+          int64_t n = row_scores(qi, kh, N, D, i, causal, scale, s);
+          row_softmax(s, n);
+          for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+          for (int64_t j = 0; j < n; ++j)
+            for (int64_t d = 0; d < D; ++d) oi[d] += s[j] * vh[j * D + d];
+          double delta = 0.0;
+          for (int64_t d = 0; d < D; ++d) delta += doi[d] * oi[d];
+          for (int64_t j = 0; j < n; ++j) {
+            const double* vj = vh + j * D;
+            double dp = 0.0;
+            for (int64_t d = 0; d < D; ++d) dp += doi[d] * vj[d];
+            double p = s[j];
+            double ds = p * (dp - delta);
+            for (int64_t d = 0; d < D; ++d) {
+              dqi[d] += scale * ds * kh[j * D + d];
+              dkh[j * D + d] += scale * ds * qi[d];
+              dvh[j * D + d] += p * doi[d];
+            }
+          }
+        }
+      }
+    }
+    free(s);
+    free(oi);
+  }
+  return err;
+}

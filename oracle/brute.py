@@ -1,0 +1,95 @@
+"""Pure-Python brute-force attention for tiny inputs (test infrastructure only).
+
+A second, independent statement of the same definitions as ``attn_oracle.c``,
+written with Python floats and ``math.fsum`` so that it shares no code path,
+compiler or summation order with the C oracle.  It exists to pin the C oracle
+on shapes small enough for nested Python loops (N, D of a few dozen at most).
+
+Definitions (FlashNystrom page, "Scope"; FlashAttention for Tesla P100 page,
+"What it supports" and "Documentation"):
+  s_ij = scale * q_i . k_j over allowed keys (j <= i when causal),
+  P_i  = softmax(s_i), O_i = sum_j P_ij v_j, LSE_i = ln sum_j exp(s_ij),
+  dS_ij = P_ij (dO_i . v_j - dO_i . O_i), dQ_i = scale sum_j dS_ij k_j,
+  dK_j = scale sum_i dS_ij q_i, dV_j = sum_i P_ij dO_i  (summed over the
+  query heads that share a key/value head).
+
+Only tests/ may import this module.
+"""
+import math
+
+
+def _idx(shape, b, h, n):
+    _, H, N, D = shape
+    return ((b * H + h) * N + n) * D
+
+
+def _row(flat, shape, b, h, n):
+    D = shape[3]
+    o = _idx(shape, b, h, n)
+    return flat[o:o + D]
+
+
+def brute_fwd(q, k, v, B, Hq, Hkv, N, D, causal, scale):
+    """q, k, v are flat Python lists of floats. Returns (o, lse) as lists."""
+    G = Hq // Hkv
+    qs, ks = (B, Hq, N, D), (B, Hkv, N, D)
+    o = [0.0] * (B * Hq * N * D)
+    lse = [0.0] * (B * Hq * N)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            for i in range(N):
+                qi = _row(q, qs, b, h, i)
+                keys = range(i + 1) if causal else range(N)
+                s = [scale * math.fsum(a * c for a, c in zip(qi, _row(k, ks, b, hk, j)))
+                     for j in keys]
+                m = max(s)
+                tot = math.fsum(math.exp(x - m) for x in s)
+                ell = m + math.log(tot)
+                p = [math.exp(x - ell) for x in s]
+                lse[(b * Hq + h) * N + i] = ell
+                base = _idx(qs, b, h, i)
+                for d in range(D):
+                    o[base + d] = math.fsum(p[t] * _row(v, ks, b, hk, j)[d]
+                                            for t, j in enumerate(keys))
+    return o, lse
+
+
+def brute_bwd(q, k, v, do, B, Hq, Hkv, N, D, causal, scale):
+    """Returns (dq, dk, dv) flat lists, from the chain rule written out."""
+    G = Hq // Hkv
+    qs, ks = (B, Hq, N, D), (B, Hkv, N, D)
+    o, _ = brute_fwd(q, k, v, B, Hq, Hkv, N, D, causal, scale)
+    dq = [0.0] * len(q)
+    dk_terms = [[] for _ in range(len(k))]
+    dv_terms = [[] for _ in range(len(v))]
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            for i in range(N):
+                qi = _row(q, qs, b, h, i)
+                doi = _row(do, qs, b, h, i)
+                oi = _row(o, qs, b, h, i)
+                keys = list(range(i + 1) if causal else range(N))
+                s = [scale * math.fsum(a * c for a, c in zip(qi, _row(k, ks, b, hk, j)))
+                     for j in keys]
+                m = max(s)
+                tot = math.fsum(math.exp(x - m) for x in s)
+                p = [math.exp(x - m) / tot for x in s]
+                delta = math.fsum(a * c for a, c in zip(doi, oi))
+                ds = []
+                for t, j in enumerate(keys):
+                    dp = math.fsum(a * c for a, c in zip(doi, _row(v, ks, b, hk, j)))
+                    ds.append(p[t] * (dp - delta))
+                qbase = _idx(qs, b, h, i)
+                for d in range(D):
+                    dq[qbase + d] = scale * math.fsum(
+                        ds[t] * _row(k, ks, b, hk, j)[d] for t, j in enumerate(keys))
+                for t, j in enumerate(keys):
+                    kbase = _idx(ks, b, hk, j)
+                    for d in range(D):
+                        dk_terms[kbase + d].append(scale * ds[t] * qi[d])
+                        dv_terms[kbase + d].append(p[t] * doi[d])
+    dk = [math.fsum(t) for t in dk_terms]
+    dv = [math.fsum(t) for t in dv_terms]
+    return dq, dk, dv
