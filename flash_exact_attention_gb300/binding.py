@@ -1,0 +1,150 @@
+"""ctypes binding of libattn.so (the C ABI in include/attn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the stream.
+There is no fallback: if the library was not built, every call raises.
+"""
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_DEVICE_TIMEOUT = 4
+ATTN_ERR_ARCH = 5
+
+_lib = None
+
+# (name, argtypes, restype) for every function include/attn.h declares.
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "attn_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_bwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
+    "attn_status_string": ([_I], ctypes.c_char_p),
+    "attn_device_status": ([_P], _I),
+    "attn_set_wait_timeout_ms": ([_I], _I),
+    "attn_version": ([], _I),
+}
+
+
+class AttnError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, status_text(status), status))
+
+
+def load():
+    """Loads libattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libattn.so is missing; build it with "
+                               "`python -m flash_exact_attention_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def status_text(status):
+    return load().attn_status_string(int(status)).decode()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# --------------------------------------------------------------- raw C names
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream=None):
+    """Raw call: pointers (ints) or tensors; returns the status code."""
+    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D,
+                           int(bool(causal)), float(scale), _stream_handle(stream))
+
+
+def attn_bwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk, dv):
+    """Raw call: pointers (ints) or tensors; returns the status code."""
+    return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D,
+                           int(bool(causal)), float(scale), _stream_handle(stream),
+                           _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
+
+
+def attn_status_string(status):
+    return status_text(status)
+
+
+def attn_device_status(stream=None):
+    return load().attn_device_status(_stream_handle(stream))
+
+
+def attn_set_wait_timeout_ms(ms):
+    return load().attn_set_wait_timeout_ms(int(ms))
+
+
+# ------------------------------------------------------- tensor conveniences
+def _check(t, shape, name):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA bf16 tensor" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def flash_attn(q, k, v, causal=False, scale=None, stream=None):
+    """O, LSE = attention(q, k, v); q [B,Hq,N,D], k/v [B,Hkv,N,D] bf16 on CUDA."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    _check(q, (B, Hq, N, D), "q")
+    _check(k, (B, Hkv, N, D), "k")
+    _check(v, (B, Hkv, N, D), "v")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    st = attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def flash_attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, stream=None):
+    """dQ, dK, dV of sum(dout * O) given the forward's O and LSE."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    for t, shp, nm in ((q, (B, Hq, N, D), "q"), (k, (B, Hkv, N, D), "k"),
+                       (v, (B, Hkv, N, D), "v"), (o, (B, Hq, N, D), "o"),
+                       (dout, (B, Hq, N, D), "dout")):
+        _check(t, shp, nm)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    st = attn_bwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk, dv)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv

@@ -1,0 +1,197 @@
+// attn_api.cu -- the C ABI of libattn.so (declared in include/attn.h): argument
+// validation, TMA tensor-map encoding, kernel dispatch and device status.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+namespace attn {
+
+// One error word per device that loads this library.  Kernels receive its
+// address as a parameter; the host reads and clears it in attn_device_status.
+__device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Signature of the driver's cuTensorMapEncodeTiled (fetched at run time so
+// that the library does not link against libcuda directly).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 wrong arch
+uint64_t g_timeout_ns = 2000ull * 1000ull * 1000ull;
+
+// Per-device setup: architecture check and the address of the error word.
+int device_setup(int* dev_out, unsigned int** err_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_arch_ok[dev] < 0) return ATTN_ERR_ARCH;
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *dev_out = dev;
+  *err_out = g_err_ptr[dev];
+  return ATTN_OK;
+}
+
+// 3-D map over a contiguous bf16 [BH, N, D] tensor: dims (D, N, BH), box
+// (64, 128, 1), 128-byte swizzle.  Rows past N inside a (batch, head) plane
+// read as zero, so a ragged tail never reads the next head.
+int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape / scale checks shared by the forward and backward.
+int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale) {
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // Element offsets use 64-bit arithmetic; grid size and TMA plane counts are
+  // 32-bit.  (B*Hq) * ceil(N/256) CTAs must fit the grid's x dimension.
+  const long long bh = (long long)B * Hq;
+  const long long qblocks = ((long long)N + 255) / 256;
+  if (bh * qblocks > 0x7FFFFFFFll || bh > 0x7FFFFFFFll) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+              int Hkv, int N, int D, int causal, float scale, void* stream) {
+  int st = validate_shape(B, Hq, Hkv, N, D, scale);
+  if (st != ATTN_OK) return st;
+  if ((long long)B * Hq * N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  unsigned int* err = nullptr;
+  st = device_setup(&dev, &err);
+  if (st != ATTN_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  if (encode_tile_map(&tq, q, D, N, B * Hq) != ATTN_OK ||
+      encode_tile_map(&tk, k, D, N, B * Hkv) != ATTN_OK ||
+      encode_tile_map(&tv, v, D, N, B * Hkv) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.G = Hq / Hkv;
+  p.num_qblocks = (N + 255) / 256;
+  p.num_kv_tiles = (N + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_timeout_ns;
+  p.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (D == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, s)
+                            : launch_fwd_d128(tq, tk, tv, p, causal != 0, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int device_status(void* stream) {
+  int dev = 0;
+  unsigned int* err = nullptr;
+  int st = device_setup(&dev, &err);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(err, 0, sizeof(word), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return word ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+int set_wait_timeout_ms(int ms) {
+  if (ms < 1) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_timeout_ns = (uint64_t)ms * 1000000ull;
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int N, int D, int causal, float scale, void* stream) {
+  return attn::fwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+             int Hq, int Hkv, int N, int D, int causal, float scale, void* stream,
+             const void* dout, void* dq, void* dk, void* dv) {
+  return attn::bwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
+                         dv);
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration (head dim must be 64 or 128)";
+    case ATTN_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case ATTN_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+int attn_device_status(void* stream) { return attn::device_status(stream); }
+
+int attn_set_wait_timeout_ms(int ms) { return attn::set_wait_timeout_ms(ms); }
+
+int attn_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,349 @@
+// fwd_kernel.cuh -- exact flash-attention forward for sm_103a (TMA + tcgen05 + TMEM).
+//
+// Work partition ("From-scratch CUDA attention kernel reaches 94.4% of
+// FlashAttention-4 on NVIDIA B200", section "How the kernel partitions its
+// work"): Q, K, V and O are cut into 128-row tiles; each CTA owns one
+// (batch, query head) and TWO consecutive 128-row Q tiles, loads them once,
+// and streams the K/V tiles of its key/value head through a shared-memory
+// ring.  For each K/V tile: S = Q K^T (tensor cores, fp32 in TMEM), an online
+// softmax update (running row max m and running row sum l, FlashStieltjes
+// page, "The challenge"), P (bf16, written back over S in TMEM), and
+// O += P V (tensor cores, fp32 in TMEM).  At the end O / l is written as bf16
+// and LSE = ln 2 * (m + log2 l).
+//
+// Warp roles (10 warps):
+//   warps 0-3  softmax for Q tile 0 (one thread per row, TMEM lanes 0-127)
+//   warps 4-7  softmax for Q tile 1
+//   warp  8    TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into the ring
+//   warp  9    TMEM allocator and tcgen05.mma issuer
+// MMA issue order per K/V tile j (two Q tiles ping-pong so that one tile's
+// softmax overlaps the other tile's matmuls):
+//   S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
+// P_t aliases S_t; tcgen05.mma operations issued by one thread execute in
+// order, so S_t(j+1) never overwrites P_t(j) before O_t += P_t(j) V_j read it.
+//
+// Softmax is computed in base 2 with c = scale * log2(e):  p = 2^(s*c - m).
+// The reference maximum m is raised only when the new row maximum exceeds it
+// by more than kRescaleThreshold (2^8); then O and l are rescaled by
+// 2^(m_old - m_new).  O and l always share the same m, so O / l and the LSE
+// are unchanged by the choice; p <= 2^8 keeps bf16/fp32 far from overflow.
+//
+// Causal (FlashAttention for Tesla P100 page, "What it supports"): tiles
+// entirely above the diagonal are skipped, not masked; only the diagonal
+// tile is masked (key > query -> -inf).  Ragged N: TMA zero-fills rows past N
+// inside each (batch, head) plane, key columns >= N are masked to -inf, and
+// rows >= N are never stored.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace attn {
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileRows = 128;
+  static constexpr int kTileBytes = kTileRows * D * 2;  // one Q/K/V tile in bf16
+  static constexpr int kBoxBytes = kTileRows * 128;     // one 64-column TMA box (128 B rows)
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = (D == 128) ? 4 : 6;
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  // barriers: q_full, full[kStages], empty[kStages], s_full[2], p_full[2], o_final
+  static constexpr int kNumBars = 1 + 2 * kStages + 5;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + misc + alignment slack
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  constexpr int ST = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_base + pad;
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+
+  const uint32_t bar0 = sbase + Cfg::kBarOff;
+  auto bar_q = [&]() { return bar0; };
+  auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (1 + ST + s); };
+  auto bar_s = [&](int t) { return bar0 + 8u * (1 + 2 * ST + t); };
+  auto bar_p = [&](int t) { return bar0 + 8u * (3 + 2 * ST + t); };
+  auto bar_o = [&]() { return bar0 + 8u * (5 + 2 * ST); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q(), 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_p(t), 4);
+    }
+    mbar_init(bar_o(), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // ---- work unit: (query block of 256 rows, batch, query head)
+  const int BH = p.B * p.Hq;
+  int qb = (int)blockIdx.x / BH;
+  if (CAUSAL) qb = p.num_qblocks - 1 - qb;  // longest rows first
+  const int bh = (int)blockIdx.x % BH;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bh_kv = b * p.Hkv + h / p.G;
+  const int q_row0 = qb * 256;
+  const bool has_t1 = q_row0 + 128 < p.N;
+  const int T = p.num_kv_tiles;
+  const int n0 = CAUSAL ? min(2 * qb + 1, T) : T;
+  const int n1 = has_t1 ? (CAUSAL ? min(2 * qb + 2, T) : T) : 0;
+  const int nkv = max(n0, n1);
+  const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int nq = has_t1 ? 2 : 1;
+      mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int c = 0; c < Cfg::kBoxes; ++c)
+          tma_load_3d(sbase + Cfg::kQOff + t * Cfg::kTileBytes + c * Cfg::kBoxBytes, &tm_q, bar_q(),
+                      c * 64, q_row0 + t * 128, bh);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv && ok; ++j) {
+        for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
+          const int s = (int)(it % ST);
+          const uint32_t ph = (it / ST) & 1u;
+          ok = mbar_wait(bar_empty(s), ph ^ 1u, wc);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_full(s), Cfg::kTileBytes);
+          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+          for (int c = 0; c < Cfg::kBoxes; ++c)
+            tma_load_3d(sbase + Cfg::kRingOff + s * Cfg::kTileBytes + c * Cfg::kBoxBytes, tm,
+                        bar_full(s), c * 64, j * 128, bh_kv);
+        }
+      }
+      if (!ok) {
+        // Let every copy already issued land before the CTA can exit.
+        for (uint32_t f = (it > (uint32_t)ST ? it - ST : 0); f < it; ++f)
+          mbar_wait_drain(bar_full((int)(f % ST)), (f / ST) & 1u, wc);
+        mbar_wait_drain(bar_q(), 0, wc);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0);
+      constexpr uint32_t kIdescO = make_idesc_bf16(128, D, 1);
+      const uint32_t q_addr[2] = {sbase + Cfg::kQOff, sbase + Cfg::kQOff + Cfg::kTileBytes};
+      const uint32_t tS[2] = {tmem_base, tmem_base + 128};
+      const uint32_t tO[2] = {tmem_base + 256, tmem_base + 384};
+      auto ring = [&](int s) { return sbase + Cfg::kRingOff + s * Cfg::kTileBytes; };
+      auto issue_qk = [&](int t, uint32_t kaddr) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
+          mma_ss(tS[t], make_sdesc_sw128(q_addr[t] + off, 16, 1024),
+                 make_sdesc_sw128(kaddr + off, 16, 1024), kIdescS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tO[t], tS[t] + kk * 8, make_sdesc_sw128(vaddr + kk * 2048, Cfg::kBoxBytes, 1024),
+                 kIdescO, (acc || kk > 0) ? 1u : 0u);
+      };
+
+      bool ok = mbar_wait(bar_q(), 0, wc);
+      uint32_t it = 0, np0 = 0, np1 = 0;
+      int sv_prev = 0;
+      bool a1_prev = false;
+      for (int j = 0; j < nkv && ok; ++j) {
+        const bool a0 = j < n0, a1 = j < n1;
+        const int sk = (int)(it % ST);
+        const uint32_t phk = (it / ST) & 1u;
+        ++it;
+        const int sv = (int)(it % ST);
+        const uint32_t phv = (it / ST) & 1u;
+        ++it;
+        if (!(ok = mbar_wait(bar_full(sk), phk, wc))) break;
+        tc_fence_after();
+        if (a0) {
+          issue_qk(0, ring(sk));
+          mma_commit(bar_s(0));
+        }
+        if (j > 0 && a1_prev) {
+          if (!(ok = mbar_wait(bar_p(1), np1 & 1u, wc))) break;
+          ++np1;
+          tc_fence_after();
+          issue_pv(1, ring(sv_prev), j - 1 > 0);
+        }
+        if (j > 0) mma_commit(bar_empty(sv_prev));
+        if (a1) {
+          issue_qk(1, ring(sk));
+          mma_commit(bar_s(1));
+        }
+        mma_commit(bar_empty(sk));
+        if (!(ok = mbar_wait(bar_full(sv), phv, wc))) break;
+        tc_fence_after();
+        if (a0) {
+          if (!(ok = mbar_wait(bar_p(0), np0 & 1u, wc))) break;
+          ++np0;
+          tc_fence_after();
+          issue_pv(0, ring(sv), j > 0);
+        }
+        sv_prev = sv;
+        a1_prev = a1;
+      }
+      if (ok && a1_prev) {
+        if ((ok = mbar_wait(bar_p(1), np1 & 1u, wc))) {
+          ++np1;
+          tc_fence_after();
+          issue_pv(1, ring(sv_prev), nkv - 1 > 0);
+        }
+      }
+      mma_commit(bar_o());
+      // On an aborted run nobody else may wait for the final commit: wait here
+      // so that no MMA is in flight when TMEM is released.
+      if (!ok) mbar_wait_drain(bar_o(), 0, wc);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int n_t = t ? n1 : n0;
+    const int qtile = 2 * qb + t;
+    const int grow = q_row0 + t * 128 + row;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + (uint32_t)(t * 128);
+    const uint32_t tO = tmem_base + lane_off + 256u + (uint32_t)(t * 128);
+    const float C = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_t; ++j) {
+      // tcgen05.ld/st are warp-collective: keep the decision warp-uniform.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), (uint32_t)j & 1u, wc));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
+      }
+      const int kv0 = j * 128;
+      if ((CAUSAL && j == qtile) || kv0 + 128 > p.N) {
+        int lim = p.N - kv0;  // columns >= lim are past the sequence end
+        if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // causal: key <= query
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_used, mx * C);
+      const bool need = (m_new - m_used) > kRescaleThreshold;
+      const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
+      if (need) m_used = m_new;
+      l *= corr;
+      const float neg_m = -m_used;
+      uint32_t pk[64];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2_approx(fmaf(s[c], C, neg_m));
+        const float p1 = ex2_approx(fmaf(s[c + 1], C, neg_m));
+        sum += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+      }
+      l += sum;
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O_t is stable here: its last update was committed before S_t(j).
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tO + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+          tmem_st32(tO + c, r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(t));
+    }
+    if (ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(), 0, wc));
+    if (ok && n_t > 0) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool live = grow < p.N;
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                             ((size_t)bh * p.N + (size_t)(live ? grow : 0)) * D);
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tO + c, r);
+        tmem_ld_wait();
+        if (live) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+            orow[c / 8 + v] = w;
+          }
+        }
+      }
+      if (live) p.lse[(size_t)bh * p.N + grow] = (m_used + log2f(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace attn

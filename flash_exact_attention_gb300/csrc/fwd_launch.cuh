@@ -1,0 +1,22 @@
+// fwd_launch.cuh -- host-side launch of fwd_kernel<D, CAUSAL> (one grid per call).
+#pragma once
+#include "fwd_kernel.cuh"
+
+namespace attn {
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, cudaStream_t stream) {
+  using Cfg = FwdCfg<D>;
+  auto kern = fwd_kernel<D, CAUSAL>;
+  // Attributes are per device; setting them on every call is cheap and keeps
+  // multi-device processes correct.
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)p.num_qblocks * (unsigned)p.B * (unsigned)p.Hq;
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

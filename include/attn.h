@@ -1,0 +1,113 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact flash attention on one NVIDIA GB300 (sm_103a).
+ *
+ * Operation (forward).  For every batch b, query head h and query row i,
+ *     O_i   = sum_j softmax_j(scale * q_i . k_j) v_j
+ *     LSE_i = ln sum_j exp(scale * q_i . k_j)
+ * over the allowed keys j (all N keys, or j <= i when causal), computed
+ * flash-style: K/V stream through on-chip tiles with a running row maximum
+ * and running row sum, and the N x N score matrix is never stored.
+ *   - exact attention and the tiling: "From-scratch CUDA attention kernel
+ *     reaches 94.4% of FlashAttention-4 on NVIDIA B200", section "How the
+ *     kernel partitions its work"; FlashNystrom page, "Scope";
+ *   - the running max / running sum: FlashStieltjes page, "The challenge";
+ *   - MHA/GQA/MQA (Hq a multiple of Hkv), causal with the upper triangle
+ *     skipped, ragged N, head dims 64 and 128, shapes (B,H,N,D):
+ *     FlashAttention for Tesla P100 page, "What it supports", "Quick start";
+ *   - LSE, the tiled softmax's running log-sum-exp state: FlashNystrom page,
+ *     "Scope" and "References".
+ * Query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Operation (backward).  Given dO = dL/dO, with P recomputed from LSE:
+ *     Delta_i = dO_i . O_i,   dS_ij = P_ij (dO_i . v_j - Delta_i)
+ *     dQ_i = scale sum_j dS_ij k_j
+ *     dK_j = scale sum_{h in group} sum_i dS_ij q_i
+ *     dV_j = sum_{h in group} sum_i P_ij dO_i
+ *   (FlashAttention for Tesla P100 page, "Documentation": dS = P(dP - D) is a
+ *   cancellation and is kept in fp32; fp32 gradient accumulation: "What it
+ *   supports".)
+ *
+ * Common conventions for every entry point.
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned, to contiguous row-major arrays:
+ *       q, o, dout, dq : bf16 [B, Hq, N, D]
+ *       k, v, dk, dv   : bf16 [B, Hkv, N, D]
+ *       lse            : fp32 [B, Hq, N]   (natural log)
+ *     bf16 means IEEE bfloat16 bit patterns (uint16 storage).
+ *   - Outputs must not alias inputs or each other.
+ *   - D must be 64 or 128; Hq must be a positive multiple of Hkv; B, N >= 0.
+ *     B*Hq*N == 0 returns ATTN_OK and launches nothing.
+ *   - scale is the softmax scale (1/sqrt(D) in the usual case); it must be
+ *     finite and positive.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: they enqueue work on the stream and never synchronise.
+ *     Argument errors are detected on the host before anything is enqueued.
+ *   - Device-side waits are bounded; a wait that runs out sets a device flag
+ *     that attn_device_status() reports (ATTN_ERR_DEVICE_TIMEOUT).
+ *   - The library keeps no per-call state; it caches the driver entry point
+ *     and kernel attributes.  It is safe to call from several host threads.
+ */
+#ifndef FLASH_EXACT_ATTENTION_GB300_ATTN_H
+#define FLASH_EXACT_ATTENTION_GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum attn_status_code {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* bad size, null pointer, misalignment, bad scale */
+  ATTN_ERR_UNSUPPORTED = 2,    /* head dim not in {64, 128} */
+  ATTN_ERR_CUDA = 3,           /* a CUDA runtime/driver call or launch failed */
+  ATTN_ERR_DEVICE_TIMEOUT = 4, /* a bounded device wait ran out (see attn_device_status) */
+  ATTN_ERR_ARCH = 5            /* the current device is not compute capability 10.3 */
+};
+
+/*
+ * Forward: writes o (bf16 [B,Hq,N,D]) and lse (fp32 [B,Hq,N]).
+ * Inputs q, k, v are read only.  Returns an attn_status_code.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int N, int D, int causal, float scale,
+             void* stream);
+
+/*
+ * Backward: the forward's arguments with o and lse as INPUTS (the outputs of
+ * attn_fwd on the same q, k, v, causal, scale), then dout (bf16 [B,Hq,N,D],
+ * input) and the outputs dq (bf16 [B,Hq,N,D]), dk, dv (bf16 [B,Hkv,N,D]).
+ * Scratch: fp32 workspaces (Delta [B,Hq,N] and a dQ accumulator
+ * [B,Hq,N,D]) are taken stream-ordered from the current device's default
+ * memory pool (cudaMallocAsync/cudaFreeAsync on `stream`).
+ * Returns an attn_status_code.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+             const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+             float scale, void* stream, const void* dout, void* dq, void* dk,
+             void* dv);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reports and clears the device-side error flag
+ * of the current device: ATTN_ERR_DEVICE_TIMEOUT if a bounded wait ran out in
+ * any kernel since the last call, ATTN_ERR_CUDA if the synchronisation
+ * failed, ATTN_OK otherwise.
+ */
+int attn_device_status(void* stream);
+
+/*
+ * Sets the limit, in milliseconds, on every device-side wait of kernels
+ * launched afterwards by this process (default 2000; values < 1 are rejected
+ * with ATTN_ERR_INVALID_ARG).
+ */
+int attn_set_wait_timeout_ms(int ms);
+
+/* Library ABI version: (major << 16) | minor. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLASH_EXACT_ATTENTION_GB300_ATTN_H */
