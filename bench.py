@@ -1,0 +1,425 @@
+"""Throughput benchmark of the exact-attention hot path on GB300.
+
+Default workload: the dense non-causal MHA configuration B=2, H=16, N=8192,
+D=128 (bf16 Q/K/V/dO iid N(0,1) from seed 0, scale = 1/sqrt(D)).  One step is
+one pass of the whole hot path over that batch: the forward (O, LSE) and,
+when the backward is built, the LSE-recompute backward (dQ, dK, dV).
+
+FLOP convention: forward 4*B*Hq*N^2*D (halved when causal), backward 2.5x the
+forward.  `value` is TFLOPS of the step (all ranks), timed with CUDA events on
+the launch stream between barriers + device synchronisation.  Inputs (256 MiB+)
+exceed the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference   # the fp64 CPU oracle on a bounded sample
+
+Prints ONE JSON line on rank 0.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOPS (bf16, fwd & fwd+bwd) and % of GB300 tensor-core peak"
+UNIT = "TFLOPS"
+
+WORKLOADS = {
+    # name: (B, Hq, Hkv, N, D, causal, description)
+    "dense_b2_h16_n8192_d128": (2, 16, 16, 8192, 128, False,
+                                "dense non-causal MHA, B=2 H=16 N=8192 D=128"),
+    "dense_b4_h16_n4096_d128": (4, 16, 16, 4096, 128, False,
+                                "dense non-causal MHA, B=4 H=16 N=4096 D=128"),
+    "dense_b1_h16_n16384_d128": (1, 16, 16, 16384, 128, False,
+                                 "dense non-causal MHA, B=1 H=16 N=16384 D=128"),
+    "causal_b1_h16_n4096_d64": (1, 16, 16, 4096, 64, True,
+                                "causal MHA training step, B=1 H=16 N=4096 D=64"),
+    "causal_gqa_b1_h8_2_n4096_d128": (1, 8, 2, 4096, 128, True,
+                                      "causal GQA, B=1 Hq=8 Hkv=2 N=4096 D=128"),
+    "causal_b1_h16_n2048_d64": (1, 16, 16, 2048, 64, True,
+                                "causal MHA, B=1 H=16 N=2048 D=64"),
+}
+DEFAULT_WORKLOAD = "dense_b2_h16_n8192_d128"
+
+
+def fwd_flops(B, Hq, N, D, causal):
+    f = 4.0 * B * Hq * N * N * D
+    return f / 2 if causal else f
+
+
+def _measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def _kernel_source_hash(names):
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "flash_exact_attention_gb300", "csrc")
+    for n in sorted(names):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+FWD_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "fwd_launch.cuh", "fwd_d128.cu", "fwd_d64.cu"]
+BWD_SOURCES = ["bwd_kernel.cuh", "ptx.cuh", "bwd.cu"]
+
+
+def _recorded_traffic(kernel, workload, src_hash):
+    """DRAM bytes per launch from profiles/dram_traffic.md, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[2] == src_hash:
+            try:
+                return float(cells[3])
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        # nvidia-smi's start-up briefly stalls the device; let it pass before timing.
+        time.sleep(1.5)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                smax = float(c[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, c[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+
+    from flash_exact_attention_gb300 import binding
+    from flash_exact_attention_gb300.synth import make_inputs, scale_for, to_torch_bf16
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    B, Hq, Hkv, N, D, causal, desc = WORKLOADS[args.workload]
+    scale = scale_for(D)
+    has_bwd = STEP_INCLUDES_BWD
+
+    x = make_inputs(B, Hq, Hkv, N, D, seed=args.seed + rank, with_do=True)
+    host = {n: to_torch_bf16(a).pin_memory() for n, a in x.items()}
+    dev = {n: t.to("cuda") for n, t in host.items()}
+    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def fwd():
+        st = binding.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, sh)
+        if st:
+            raise binding.AttnError(st, "attn_fwd")
+
+    def bwd():
+        st = binding.attn_bwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, sh, do, dq, dk,
+                              dv)
+        if st:
+            raise binding.AttnError(st, "attn_bwd")
+
+    def step():
+        fwd()
+        if has_bwd:
+            bwd()
+
+    launches_per_step = 1 + (BWD_LAUNCHES if has_bwd else 0)
+    ff = fwd_flops(B, Hq, N, D, causal)
+    step_flops = ff * (3.5 if has_bwd else 1.0)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    st = binding.attn_device_status(sh)
+    if st:
+        raise binding.AttnError(st, "warm-up")
+
+    # ---- timed region: whole steps, CUDA events on the launch stream
+    with ClockSampler(local) as clk:
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+        ms_total = e0.elapsed_time(e1)
+        # per-kernel timing of the forward (the roofline's kernel), same stream
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            fwd()
+        f1.record(stream)
+        barrier()
+        ms_fwd = f0.elapsed_time(f1)
+    st = binding.attn_device_status(sh)
+    if st:
+        raise binding.AttnError(st, "timed region")
+
+    ms_step = ms_total / args.steps
+    ms_fwd_launch = ms_fwd / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step, ms_fwd_launch], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_fwd_launch = float(t[0]), float(t[1])
+    value = ws * step_flops / (ms_step * 1e-3) / 1e12
+    fwd_tflops = ff / (ms_fwd_launch * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    out_names = ["o", "lse"] + (["dq", "dk", "dv"] if has_bwd else [])
+    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    host_out = {n: torch.empty(outs[n].shape, dtype=outs[n].dtype, pin_memory=True)
+                for n in out_names}
+    in_names = ["q", "k", "v"] + (["do"] if has_bwd else [])
+    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
+    d2h = sum(host_out[n].numel() * host_out[n].element_size() for n in out_names)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(e2e_steps):
+        for n in in_names:
+            dev[n].copy_(host[n], non_blocking=True)
+        step()
+        for n in out_names:
+            host_out[n].copy_(outs[n], non_blocking=True)
+    g1.record(stream)
+    barrier()
+    ms_e2e = g0.elapsed_time(g1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t[0])
+    e2e_value = ws * step_flops / (ms_e2e * 1e-3) / 1e12
+
+    peak_burst, peak_sust, peak_src = _measured_peaks()
+    fwd_kernel_name = "fwd_kernel<%d,%s>" % (D, "causal" if causal else "noncausal")
+    src_hash = _kernel_source_hash(FWD_SOURCES)
+    traffic = _recorded_traffic(fwd_kernel_name, args.workload, src_hash)
+    roofline = {"bound": "tensor", "achieved": round(fwd_tflops, 1), "peak": peak_burst,
+                "unit": "TFLOP/s", "frac": round(fwd_tflops / peak_burst, 4),
+                "traffic": traffic, "kernel": fwd_kernel_name,
+                "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_src
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                "frac_of_sustained": round(fwd_tflops / peak_sust, 4),
+                "algorithmic_flops_per_launch": ff, "source_hash": src_hash}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic iid N(0,1) bf16 from numpy seed %d (+rank)" % args.seed,
+        "config": {"workload": desc, "name": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv,
+                   "N": N, "D": D, "causal": causal,
+                   "step": "fwd+bwd" if has_bwd else "fwd (backward not built)",
+                   "parallelism": "replicas" if ws == 1 else "dp%d (independent batches)" % ws,
+                   "l2": "no flush: per-step inputs %.0f MiB exceed the 129 MB L2"
+                         % ((h2d + o.numel() * 2) / 2**20)},
+        "fwd_tflops": round(fwd_tflops, 1),
+        "fwd_pct_of_peak": round(100 * fwd_tflops / peak_burst, 2),
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.workload, has_bwd, args.cpu_seconds)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# Kernels the backward launches per call, and whether a step includes it.
+BWD_LAUNCHES = 3
+STEP_INCLUDES_BWD = False
+
+
+def cpu_baseline(workload, with_bwd, budget_s):
+    """The fp64 oracle, as it stands, on a bounded sample of the same workload."""
+    import numpy as np
+
+    import oracle
+    from flash_exact_attention_gb300.synth import bf16_bits_to_f32, make_inputs, scale_for
+
+    B, Hq, Hkv, N, D, causal, _ = WORKLOADS[workload]
+    scale = scale_for(D)
+    x = make_inputs(B, Hq, Hkv, N, D, seed=0, with_do=with_bwd)
+    q, k, v = (bf16_bits_to_f32(x[n]) for n in ("q", "k", "v"))
+    rng = np.random.default_rng(1)
+    flops = 0.0
+    t0 = time.perf_counter()
+    rows_done = 0
+    # forward on random rows in batches until the time budget is spent
+    fwd_budget = budget_s / (3.5 if with_bwd else 1.0)
+    while time.perf_counter() - t0 < fwd_budget:
+        rows = rng.integers(0, B * Hq * N, size=max(64, oracle.num_threads() * 16))
+        oracle.fwd_rows(q, k, v, causal, scale, rows)
+        i = rows % N
+        keys = (i + 1) if causal else np.full_like(i, N)
+        flops += float(np.sum(4.0 * keys * D))
+        rows_done += rows.size
+    t_fwd = time.perf_counter() - t0
+    sample = "forward of %d random rows" % rows_done
+    t_bwd = 0.0
+    if with_bwd:
+        # backward of the first (batch, kv-head) group of the same workload
+        t1 = time.perf_counter()
+        sl = slice(0, Hq // Hkv)
+        qq = q[:1, sl]
+        kk = k[:1, :1]
+        vv = v[:1, :1]
+        dd = bf16_bits_to_f32(x["do"])[:1, sl]
+        oracle.bwd(qq, kk, vv, dd, causal, scale)
+        t_bwd = time.perf_counter() - t1
+        flops += 2.5 * fwd_flops(1, Hq // Hkv, N, D, causal)
+        sample += " + backward of one (batch, kv-head) group (%d query heads)" % (Hq // Hkv)
+    secs = t_fwd + t_bwd
+    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT,
+            "cores": oracle.num_threads(), "kind": "oracle", "sample": sample,
+            "seconds": round(secs, 2), "host_cpus": os.cpu_count()}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    has_bwd = STEP_INCLUDES_BWD
+    B, Hq, Hkv, N, D, causal, desc = WORKLOADS[args.workload]
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_baseline(args.workload, has_bwd, 0.2)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(args.workload, has_bwd, args.cpu_seconds / max(1, args.steps)))
+    wall = time.perf_counter() - t0
+    value = statistics.median(v["value"] for v in vals)
+    cb = dict(vals[-1])
+    cb["value"] = value
+    result = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * wall / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic iid N(0,1) bf16 from numpy seed 0",
+        "config": {"workload": desc, "name": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv,
+                   "N": N, "D": D, "causal": causal,
+                   "step": "fwd+bwd" if has_bwd else "fwd",
+                   "note": "the fp64 CPU oracle on a bounded sample of the workload per step"},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall-clock budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()
