@@ -34,7 +34,8 @@
  *
  * All inputs are fp64 arrays (the caller widens bf16 exactly).  Layouts are
  * contiguous [B, H, N, D] row-major; lse is [B, Hq, N].  OpenMP parallelises
- * over independent rows (forward) and over (batch, kv-head) groups (backward).
+ * over independent rows (forward) and over the query rows of one (batch, kv-head)
+ * group at a time (backward).
  */
 #include <math.h>
 #include <stdint.h>
@@ -135,62 +136,78 @@ int oracle_fwd_rows(const double* q, const double* k, const double* v,
  *   dQ_i = scale sum_j dS_ij k_j
  *   dK_j = scale sum_{h in group} sum_i dS_ij q_i
  *   dV_j = sum_{h in group} sum_i P_ij dO_i
- * One OpenMP task per (b, kv-head) so dK/dV have a single writer.
+ * The (batch, kv-head) groups run one after another; inside a group OpenMP
+ * splits the query rows of all its heads, each thread summing its rows' dK/dV
+ * terms privately before one reduction per group.
  */
 int oracle_bwd(const double* q, const double* k, const double* v, const double* dout,
                int B, int Hq, int Hkv, int N, int D, int causal, double scale,
                double* dq, double* dk, double* dv) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || D <= 0 || Hq % Hkv) return -1;
   const int64_t G = Hq / Hkv;
+  const int64_t ND = (int64_t)N * D;
   memset(dq, 0, sizeof(double) * (size_t)B * Hq * N * D);
   memset(dk, 0, sizeof(double) * (size_t)B * Hkv * N * D);
   memset(dv, 0, sizeof(double) * (size_t)B * Hkv * N * D);
   int err = 0;
+  for (int64_t g = 0; g < (int64_t)B * Hkv && !err; ++g) {
+    const int64_t b = g / Hkv, hk = g % Hkv;
+    const double* kh = k + at4(b, hk, 0, 0, Hkv, N, D);
+    const double* vh = v + at4(b, hk, 0, 0, Hkv, N, D);
+    double* dkh = dk + at4(b, hk, 0, 0, Hkv, N, D);
+    double* dvh = dv + at4(b, hk, 0, 0, Hkv, N, D);
 #pragma omp parallel
-  {
-    double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
-    double* oi = (double*)malloc(sizeof(double) * D);
-    if (!s || !oi) {
+    {
+      double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+      double* oi = (double*)malloc(sizeof(double) * D);
+      double* dkp = (double*)calloc((size_t)(ND > 0 ? ND : 1), sizeof(double));
+      double* dvp = (double*)calloc((size_t)(ND > 0 ? ND : 1), sizeof(double));
+      const int have = s && oi && dkp && dvp;
+      if (!have) {
 #pragma omp atomic write
-      err = -1;
-    }
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t g = 0; g < (int64_t)B * Hkv; ++g) {
-      if (!s || !oi) continue;
-      int64_t b = g / Hkv, hk = g % Hkv;
-      const double* kh = k + at4(b, hk, 0, 0, Hkv, N, D);
-      const double* vh = v + at4(b, hk, 0, 0, Hkv, N, D);
-      double* dkh = dk + at4(b, hk, 0, 0, Hkv, N, D);
-      double* dvh = dv + at4(b, hk, 0, 0, Hkv, N, D);
-      for (int64_t h = hk * G; h < (hk + 1) * G; ++h) {
-        for (int64_t i = 0; i < N; ++i) {
-          const double* qi = q + at4(b, h, i, 0, Hq, N, D);
-          const double* doi = dout + at4(b, h, i, 0, Hq, N, D);
-          double* dqi = dq + at4(b, h, i, 0, Hq, N, D);
-          int64_t n = row_scores(qi, kh, N, D, i, causal, scale, s);
-          row_softmax(s, n);
-          for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
-          for (int64_t j = 0; j < n; ++j)
-            for (int64_t d = 0; d < D; ++d) oi[d] += s[j] * vh[j * D + d];
-          double delta = 0.0;
-          for (int64_t d = 0; d < D; ++d) delta += doi[d] * oi[d];
-          for (int64_t j = 0; j < n; ++j) {
-            const double* vj = vh + j * D;
-            double dp = 0.0;
-            for (int64_t d = 0; d < D; ++d) dp += doi[d] * vj[d];
-            double p = s[j];
-            double ds = p * (dp - delta);
-            for (int64_t d = 0; d < D; ++d) {
-              dqi[d] += scale * ds * kh[j * D + d];
-              dkh[j * D + d] += scale * ds * qi[d];
-              dvh[j * D + d] += p * doi[d];
-            }
+        err = -1;
+      }
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t r = 0; r < G * N; ++r) {
+        if (!have) continue;
+        const int64_t h = hk * G + r / N, i = r % N;
+        const double* qi = q + at4(b, h, i, 0, Hq, N, D);
+        const double* doi = dout + at4(b, h, i, 0, Hq, N, D);
+        double* dqi = dq + at4(b, h, i, 0, Hq, N, D);
+        int64_t n = row_scores(qi, kh, N, D, i, causal, scale, s);
+        row_softmax(s, n);
+        for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+          for (int64_t d = 0; d < D; ++d) oi[d] += s[j] * vh[j * D + d];
+        double delta = 0.0;
+        for (int64_t d = 0; d < D; ++d) delta += doi[d] * oi[d];
+        for (int64_t j = 0; j < n; ++j) {
+          const double* vj = vh + j * D;
+          double dp = 0.0;
+          for (int64_t d = 0; d < D; ++d) dp += doi[d] * vj[d];
+          double p = s[j];
+          double ds = p * (dp - delta);
+          for (int64_t d = 0; d < D; ++d) {
+            dqi[d] += scale * ds * kh[j * D + d];
+            dkp[j * D + d] += scale * ds * qi[d];
+            dvp[j * D + d] += p * doi[d];
           }
         }
       }
+      if (have) {
+#pragma omp critical
+        {
+          for (int64_t e = 0; e < ND; ++e) {
+            dkh[e] += dkp[e];
+            dvh[e] += dvp[e];
+          }
+        }
+      }
+      free(s);
+      free(oi);
+      free(dkp);
+      free(dvp);
     }
-    free(s);
-    free(oi);
   }
   return err;
 }
