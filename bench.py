@@ -76,7 +76,8 @@ def _kernel_source_hash(names):
 
 
 FWD_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "fwd_launch.cuh", "fwd_d128.cu", "fwd_d64.cu"]
-BWD_SOURCES = ["bwd_kernel.cuh", "ptx.cuh", "bwd.cu"]
+BWD_SOURCES = ["bwd_kernel.cuh", "ptx.cuh", "bwd_launch.cuh", "bwd.cu", "bwd_d128.cu",
+               "bwd_d64.cu"]
 
 
 def _recorded_traffic(kernel, workload, src_hash):
@@ -226,27 +227,40 @@ def run_native(args):
         e1.record(stream)
         barrier()
         ms_total = e0.elapsed_time(e1)
-        # per-kernel timing of the forward (the roofline's kernel), same stream
+        # per-part timing on the same stream: forward calls, then backward calls
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for _ in range(args.steps):
             fwd()
         f1.record(stream)
+        ms_fwd = 0.0
+        ms_bwd = 0.0
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        if has_bwd:
+            b0.record(stream)
+            for _ in range(args.steps):
+                bwd()
+            b1.record(stream)
         barrier()
         ms_fwd = f0.elapsed_time(f1)
+        if has_bwd:
+            ms_bwd = b0.elapsed_time(b1)
     st = binding.attn_device_status(sh)
     if st:
         raise binding.AttnError(st, "timed region")
 
     ms_step = ms_total / args.steps
     ms_fwd_launch = ms_fwd / args.steps
+    ms_bwd_call = ms_bwd / args.steps
     if dist is not None:
-        t = torch.tensor([ms_step, ms_fwd_launch], device="cuda")
+        t = torch.tensor([ms_step, ms_fwd_launch, ms_bwd_call], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd_launch = float(t[0]), float(t[1])
+        ms_step, ms_fwd_launch, ms_bwd_call = float(t[0]), float(t[1]), float(t[2])
     value = ws * step_flops / (ms_step * 1e-3) / 1e12
     fwd_tflops = ff / (ms_fwd_launch * 1e-3) / 1e12
+    bwd_tflops = 2.5 * ff / (ms_bwd_call * 1e-3) / 1e12 if has_bwd else None
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     out_names = ["o", "lse"] + (["dq", "dk", "dv"] if has_bwd else [])
@@ -277,17 +291,26 @@ def run_native(args):
     e2e_value = ws * step_flops / (ms_e2e * 1e-3) / 1e12
 
     peak_burst, peak_sust, peak_src = _measured_peaks()
-    fwd_kernel_name = "fwd_kernel<%d,%s>" % (D, "causal" if causal else "noncausal")
-    src_hash = _kernel_source_hash(FWD_SOURCES)
-    traffic = _recorded_traffic(fwd_kernel_name, args.workload, src_hash)
-    roofline = {"bound": "tensor", "achieved": round(fwd_tflops, 1), "peak": peak_burst,
-                "unit": "TFLOP/s", "frac": round(fwd_tflops / peak_burst, 4),
-                "traffic": traffic, "kernel": fwd_kernel_name,
-                "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_src
-                if peak_src == "measured" else "fallback 1.9 PFLOP/s",
-                "frac_of_sustained": round(fwd_tflops / peak_sust, 4),
-                "algorithmic_flops_per_launch": ff, "source_hash": src_hash}
+    peak_note = ("%s bf16 burst (MEASURED_PEAKS.json)" % peak_src if peak_src == "measured"
+                 else "fallback 1.9 PFLOP/s")
+    tag = "%d,%s" % (D, "causal" if causal else "noncausal")
 
+    def roof(kernel, sources, tflops, flops):
+        h = _kernel_source_hash(sources)
+        return {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak_burst,
+                "unit": "TFLOP/s", "frac": round(tflops / peak_burst, 4),
+                "traffic": _recorded_traffic(kernel, args.workload, h), "kernel": kernel,
+                "peak_source": peak_note, "frac_of_sustained": round(tflops / peak_sust, 4),
+                "algorithmic_flops_per_launch": flops, "source_hash": h}
+
+    roof_fwd = roof("fwd_kernel<%s>" % tag, FWD_SOURCES, fwd_tflops, ff)
+    if has_bwd:
+        # The backward call (preprocess + main + postprocess, timed together) is
+        # the dominant part of the step; its FLOPs are the main kernel's.
+        roofline = roof("bwd_kernel<%s>" % tag, BWD_SOURCES, bwd_tflops, 2.5 * ff)
+        roofline["timed_as"] = "whole attn_bwd call (3 launches)"
+    else:
+        roofline = roof_fwd
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -301,7 +324,9 @@ def run_native(args):
                          % ((h2d + o.numel() * 2) / 2**20)},
         "fwd_tflops": round(fwd_tflops, 1),
         "fwd_pct_of_peak": round(100 * fwd_tflops / peak_burst, 2),
+        "bwd_tflops": round(bwd_tflops, 1) if has_bwd else None,
         "roofline": roofline,
+        "roofline_fwd": roof_fwd,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -318,7 +343,7 @@ def run_native(args):
 
 # Kernels the backward launches per call, and whether a step includes it.
 BWD_LAUNCHES = 3
-STEP_INCLUDES_BWD = False
+STEP_INCLUDES_BWD = True
 
 
 def cpu_baseline(workload, with_bwd, budget_s):

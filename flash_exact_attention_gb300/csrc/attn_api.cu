@@ -34,6 +34,13 @@ unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 wrong arch
 uint64_t g_timeout_ns = 2000ull * 1000ull * 1000ull;
 
+}  // namespace
+
+uint64_t wait_timeout_ns() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_timeout_ns;
+}
+
 // Per-device setup: architecture check and the address of the error word.
 int device_setup(int* dev_out, unsigned int** err_out) {
   int dev = 0;
@@ -82,8 +89,6 @@ int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 // Shape / scale checks shared by the forward and backward.
 int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale) {
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_INVALID_ARG;
@@ -94,11 +99,10 @@ int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale) {
   // 32-bit.  (B*Hq) * ceil(N/256) CTAs must fit the grid's x dimension.
   const long long bh = (long long)B * Hq;
   const long long qblocks = ((long long)N + 255) / 256;
-  if (bh * qblocks > 0x7FFFFFFFll || bh > 0x7FFFFFFFll) return ATTN_ERR_INVALID_ARG;
+  if (bh * qblocks * 2 > 0x7FFFFFFFll || bh > 0x7FFFFFFFll) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
-}  // namespace
 
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
               int Hkv, int N, int D, int causal, float scale, void* stream) {
@@ -130,7 +134,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.num_qblocks = (N + 255) / 256;
   p.num_kv_tiles = (N + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.timeout_ns = g_timeout_ns;
+  p.timeout_ns = wait_timeout_ns();
   p.err = err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = (D == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, s)

@@ -1,0 +1,418 @@
+// bwd_kernel.cuh -- exact flash-attention backward for sm_103a (TMA + tcgen05 + TMEM).
+//
+// P is recomputed from the forward's row log-sum-exp, never stored; dS = P o (dP - Delta)
+// with Delta_i = dO_i . O_i is formed in fp32 (FlashAttention for Tesla P100
+// page, "Documentation": dS is a cancellation, dV = P^T dO is not).  Gradients
+// accumulate in fp32 ("What it supports": fp32 gradient accumulation).
+//
+// Three kernels per call:
+//   bwd_preprocess  Delta_i = sum_d dO_id O_id and LSE2_i = LSE_i log2(e), written
+//                   to row-padded buffers (rows past N: LSE2 = +inf so P = 0,
+//                   Delta = 0); zeroes the fp32 dQ accumulator.
+//   bwd_kernel      one CTA per (batch, kv head, 128-key tile j).  It loops over
+//                   the query heads of its group and over the query tiles i
+//                   (i >= j when causal: tiles above the diagonal are skipped):
+//                     S^T  = K_j Q_i^T            (tcgen05, TMEM, keys on lanes)
+//                     dP^T = V_j dO_i^T           (tcgen05, TMEM)
+//                     P^T  = 2^(S^T c - LSE2_i), dS^T = P^T o (dP^T - Delta_i)
+//                     dV_j += P^T dO_i            (A = P^T from TMEM)
+//                     dK_j += dS^T Q_i            (A = dS^T from shared memory)
+//                     dQ_i  = dS K_j              (A = the same dS^T tile read MN-major)
+//                   dK/dV stay in TMEM across the whole group (no GQA reduction
+//                   pass); dQ_i is added to the fp32 accumulator with vector
+//                   reductions by a dedicated warpgroup.
+//   bwd_postprocess dQ = scale * dQacc -> bf16.
+//
+// Warp roles of bwd_kernel (10 warps): 0-3 dS (one thread per key row) and the
+// dK/dV epilogue; 4-7 dQ reduction (one thread per query row); 8 TMA producer
+// (K_j, V_j once; Q_i, dO_i, LSE2, Delta per iteration into a 2-stage ring);
+// 9 TMEM allocator and MMA issuer.
+//
+// TMEM columns: [0,128) S^T, with P^T (bf16) written over its first 64;
+// [128,256) dP^T, later overwritten by dQ_i; [256,256+D) dV; [256+D,256+2D) dK.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace attn {
+
+constexpr unsigned kErrSmemAlign = 2u;  // device error bit: shared memory base misaligned
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTile = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kBox = 128 * 128;     // one 64-column box (128-byte rows)
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kK = 0;
+  static constexpr int kV = kTile;
+  static constexpr int kQ0 = 2 * kTile;      // stage s: Q at kQ0 + s*2*kTile, dO right after
+  static constexpr int kdS = 6 * kTile;      // dS^T tile: 128 keys x 128 queries bf16
+  static constexpr int kVec = kdS + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
+  static constexpr int kBar = kVec + 2 * 1024;
+  // kv_full, qd_full[2], qd_empty[2], s_ready, ds_ready, dq_ready, dq_free, all_done
+  static constexpr int kNumBars = 10;
+  static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  // The 128-byte swizzle atoms need a 1024-byte aligned base; there is no room
+  // for padding at D=128, so refuse (and report) instead of computing garbage.
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrSmemAlign);
+    return;
+  }
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+
+  const uint32_t bar0 = sbase + Cfg::kBar;
+  const uint32_t bar_kv = bar0;
+  auto bar_qd_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_qd_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  const uint32_t bar_s = bar0 + 8u * 5;
+  const uint32_t bar_ds = bar0 + 8u * 6;
+  const uint32_t bar_dq = bar0 + 8u * 7;
+  const uint32_t bar_dq_free = bar0 + 8u * 8;
+  const uint32_t bar_done = bar0 + 8u * 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBar + Cfg::kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_qd_full(s), 1);
+      mbar_init(bar_qd_empty(s), 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_ds, 4);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_dq_free, 4);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // ---- work unit: (key tile j, batch, kv head); heaviest key tiles first when causal
+  const int BHkv = p.B * p.Hkv;
+  const int j = (int)blockIdx.x / BHkv;
+  const int bhkv = (int)blockIdx.x % BHkv;
+  const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
+  const int T = p.num_kv_tiles;
+  const int i0 = CAUSAL ? j : 0;
+  const int n_i = T - i0;
+  const int n_it = p.G * n_i;
+  auto q_head = [&](int it) { return b * p.Hq + hkv * p.G + it / n_i; };  // flat b*Hq + h
+  auto q_tile = [&](int it) { return i0 + it % n_i; };
+  const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
+  const uint32_t tS = tmem_base, tdP = tmem_base + 128, tdV = tmem_base + 256,
+                 tdK = tmem_base + 256 + D;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_kv, 2 * Cfg::kTile);
+      for (int c = 0; c < Cfg::kBoxes; ++c) {
+        tma_load_3d(sbase + Cfg::kK + c * Cfg::kBox, &tm_k, bar_kv, c * 64, j * 128, bhkv);
+        tma_load_3d(sbase + Cfg::kV + c * Cfg::kBox, &tm_v, bar_kv, c * 64, j * 128, bhkv);
+      }
+      int it = 0;
+      bool ok = true;
+      for (; it < n_it; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(bar_qd_empty(s), ((uint32_t)(it >> 1) & 1u) ^ 1u, wc))) break;
+        const int bhq = q_head(it), i = q_tile(it);
+        const uint32_t qs = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
+        mbar_arrive_expect_tx(bar_qd_full(s), 2 * Cfg::kTile + 1024);
+        for (int c = 0; c < Cfg::kBoxes; ++c) {
+          tma_load_3d(qs + c * Cfg::kBox, &tm_q, bar_qd_full(s), c * 64, i * 128, bhq);
+          tma_load_3d(qs + Cfg::kTile + c * Cfg::kBox, &tm_do, bar_qd_full(s), c * 64, i * 128,
+                      bhq);
+        }
+        const size_t voff = (size_t)bhq * p.Npad + (size_t)i * 128;
+        bulk_load(sbase + Cfg::kVec + s * 1024, p.lse2 + voff, 512, bar_qd_full(s));
+        bulk_load(sbase + Cfg::kVec + s * 1024 + 512, p.delta + voff, 512, bar_qd_full(s));
+      }
+      if (!ok) {
+        for (int f = (it > 2 ? it - 2 : 0); f < it; ++f)
+          mbar_wait_drain(bar_qd_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
+        mbar_wait_drain(bar_kv, 0, wc);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t kIdescB_MN = make_idesc_bf16(128, D, 1, 0);  // dV, dK
+      constexpr uint32_t kIdescDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A and B MN-major
+      const uint32_t k_addr = sbase + Cfg::kK, v_addr = sbase + Cfg::kV, ds_addr = sbase + Cfg::kdS;
+      auto q_addr = [&](int s) { return sbase + Cfg::kQ0 + s * 2 * Cfg::kTile; };
+      auto do_addr = [&](int s) { return sbase + Cfg::kQ0 + s * 2 * Cfg::kTile + Cfg::kTile; };
+      // X^T = A B^T with A a [128 x D] K-major tile (K or V), B a [128 x D] K-major tile.
+      auto issue_t = [&](uint32_t dst, uint32_t a, uint32_t bb) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * Cfg::kBox + (kk % 4) * 32;
+          mma_ss(dst, make_sdesc_sw128(a + off, 16, 1024), make_sdesc_sw128(bb + off, 16, 1024),
+                 kIdescSS, kk > 0);
+        }
+      };
+      auto issue_grads = [&](int s, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO  (K = 128 queries)
+          mma_ts(tdV, tS + kk * 8, make_sdesc_sw128(do_addr(s) + kk * 2048, Cfg::kBox, 1024),
+                 kIdescB_MN, (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q  (K = 128 queries)
+          const uint32_t off = (kk / 4) * Cfg::kBox + (kk % 4) * 32;
+          mma_ss(tdK, make_sdesc_sw128(ds_addr + off, 16, 1024),
+                 make_sdesc_sw128(q_addr(s) + kk * 2048, Cfg::kBox, 1024), kIdescB_MN,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys), into the dP^T columns
+          mma_ss(tdP, make_sdesc_sw128(ds_addr + kk * 2048, Cfg::kBox, 1024),
+                 make_sdesc_sw128(k_addr + kk * 2048, Cfg::kBox, 1024), kIdescDQ, kk > 0);
+      };
+
+      bool ok = mbar_wait(bar_kv, 0, wc) && mbar_wait(bar_qd_full(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_t(tS, k_addr, q_addr(0));
+        issue_t(tdP, v_addr, do_addr(0));
+        mma_commit(bar_s);
+      }
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(bar_ds, (uint32_t)it & 1u, wc))) break;
+        tc_fence_after();
+        issue_grads(s, it > 0);
+        mma_commit(bar_dq);
+        mma_commit(bar_qd_empty(s));
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) & 1;
+          if (!(ok = mbar_wait(bar_qd_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
+          tc_fence_after();
+          issue_t(tS, k_addr, q_addr(s1));
+          if (!(ok = mbar_wait(bar_dq_free, (uint32_t)it & 1u, wc))) break;
+          tc_fence_after();
+          issue_t(tdP, v_addr, do_addr(s1));
+          mma_commit(bar_s);
+        }
+      }
+      mma_commit(bar_done);
+      if (!ok) mbar_wait_drain(bar_done, 0, wc);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ dQ reduction
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // query row within the tile
+    const uint32_t tq = tdP + ((uint32_t)(wq * 32) << 16);
+    for (int it = 0; it < n_it; ++it) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, (uint32_t)it & 1u, wc))) break;
+      tc_fence_after();
+      uint32_t r[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tq + c * 32, r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_free);
+      // Rows past N belong to the padded accumulator and receive zeros.
+      float* dst = p.dq_acc + ((size_t)q_head(it) * p.Npad + (size_t)q_tile(it) * 128 + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          red_add_v4(dst + c * 32 + v * 4, __uint_as_float(r[c][4 * v]),
+                     __uint_as_float(r[c][4 * v + 1]), __uint_as_float(r[c][4 * v + 2]),
+                     __uint_as_float(r[c][4 * v + 3]));
+    }
+  } else {
+    // ------------------------------------------------------------ dS = P o (dP - Delta)
+    const int row = warp * 32 + lane;  // key row within the tile
+    const int kj = j * 128 + row;
+    const bool key_live = kj < p.N;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float C = p.scale_log2;
+    const uint32_t ds_row = sbase + Cfg::kdS + (uint32_t)row * 128u;
+    const uint32_t swz = (uint32_t)(row & 7);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)it & 1u, wc) &&
+                                       mbar_wait(bar_qd_full(s), (uint32_t)(it >> 1) & 1u, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kVec + s * 1024);
+      const float* delta = lse2 + 128;
+      const bool diag = CAUSAL && q_tile(it) == j;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 32 query columns at a time
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + lane_off + c * 32, sr);
+        tmem_ld32(tdP + lane_off + c * 32, dr);
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int qc = c * 32 + e;
+          const float2 l2 = *reinterpret_cast<const float2*>(lse2 + qc);
+          const float2 dl = *reinterpret_cast<const float2*>(delta + qc);
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), C, -l2.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), C, -l2.y));
+          if (diag) {  // causal: query < key is masked
+            if (qc < row) p0 = 0.f;
+            if (qc + 1 < row) p1 = 0.f;
+          }
+          if (!key_live) p0 = p1 = 0.f;
+          const float d0 = p0 * (__uint_as_float(dr[e]) - dl.x);
+          const float d1 = p1 * (__uint_as_float(dr[e + 1]) - dl.y);
+          pk[e / 2] = pack_bf16x2(p0, p1);
+          dk[e / 2] = pack_bf16x2(d0, d1);
+        }
+        // P^T (bf16) over S^T columns already read: chunk c fills columns [16c, 16c+16).
+        tmem_st16(tS + lane_off + c * 16, pk);
+        // dS^T row to shared memory in the 128-byte swizzled layout.
+        const uint32_t box = ds_row + (uint32_t)(c >> 1) * Cfg::kBox;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t chunk = ((uint32_t)((c & 1) * 4 + v)) ^ swz;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + chunk * 16),
+                       "r"(dk[4 * v]), "r"(dk[4 * v + 1]), "r"(dk[4 * v + 2]), "r"(dk[4 * v + 3])
+                       : "memory");
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, wc));
+    if (ok) {
+      tc_fence_after();
+      const size_t orow = ((size_t)bhkv * p.N + (size_t)(key_live ? kj : 0)) * D;
+      uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + orow);
+      uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + orow);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which ? p.scale : 1.f;
+        uint4* out = which ? dk : dv;
+        const uint32_t src = (which ? tdK : tdV) + lane_off;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(src + c * 32, r);
+          tmem_ld_wait();
+          if (key_live) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * mul, __uint_as_float(r[8 * v + 1]) * mul);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * mul, __uint_as_float(r[8 * v + 3]) * mul);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * mul, __uint_as_float(r[8 * v + 5]) * mul);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * mul, __uint_as_float(r[8 * v + 7]) * mul);
+              out[c * 4 + v] = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// Delta and LSE2 into row-padded buffers; zero the dQ accumulator.  One warp per
+// padded row (b*Hq + h, i), i < Npad.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                   const float* __restrict__ lse, float* __restrict__ lse2,
+                   float* __restrict__ delta, float* __restrict__ dq_acc, long long rows, int N,
+                   int Npad) {
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const long long bh = r / Npad;
+  const int i = (int)(r % Npad);
+  float acc = 0.f;
+  if (i < N) {
+    constexpr int kPer = D / 32;  // elements per lane: 2 or 4
+    const size_t base = ((size_t)bh * N + i) * D + (size_t)lane * kPer;
+    if (kPer == 2) {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
+      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dout + base);
+      acc = __bfloat162float(a.x) * __bfloat162float(g.x) + __bfloat162float(a.y) * __bfloat162float(g.y);
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+      const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        acc += __bfloat162float(a2[t].x) * __bfloat162float(g2[t].x) +
+               __bfloat162float(a2[t].y) * __bfloat162float(g2[t].y);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  }
+  if (lane == 0) {
+    lse2[r] = i < N ? lse[(size_t)bh * N + i] * 1.4426950408889634f : INFINITY;
+    delta[r] = acc;
+  }
+  float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)r * D);
+#pragma unroll
+  for (int t = lane; t < D / 4; t += 32) z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = scale * dQacc (rows < N) -> bf16.  8 elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_postprocess(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                    long long rows, int N, int Npad, float scale) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element group
+  constexpr int kGroups = D / 8;
+  const long long r = idx / kGroups;  // output row (b*Hq + h)*N + i
+  if (r >= rows) return;
+  const int g = (int)(idx % kGroups);
+  const long long bh = r / N;
+  const int i = (int)(r % N);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Npad + i) * D + g * 8);
+  const float4 a = src[0], c = src[1];
+  uint4 w;
+  w.x = pack_bf16x2(a.x * scale, a.y * scale);
+  w.y = pack_bf16x2(a.z * scale, a.w * scale);
+  w.z = pack_bf16x2(c.x * scale, c.y * scale);
+  w.w = pack_bf16x2(c.z * scale, c.w * scale);
+  reinterpret_cast<uint4*>(dq + (size_t)r * D)[g] = w;
+}
+
+}  // namespace attn

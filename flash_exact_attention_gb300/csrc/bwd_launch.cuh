@@ -1,0 +1,32 @@
+// bwd_launch.cuh -- host-side launch of the three backward kernels for one head dim.
+#pragma once
+#include "bwd_kernel.cuh"
+
+namespace attn {
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, const void* o,
+                            const void* dout, const float* lse, void* dq, cudaStream_t stream) {
+  using Cfg = BwdCfg<D>;
+  const long long prow = (long long)p.B * p.Hq * p.Npad;  // padded rows
+  bwd_preprocess<D><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse,
+      const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dq_acc, prow, p.N, p.Npad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kern = bwd_kernel<D, CAUSAL>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long orow = (long long)p.B * p.Hq * p.N;
+  const long long groups = orow * (D / 8);
+  bwd_postprocess<D><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
+      p.dq_acc, static_cast<__nv_bfloat16*>(dq), orow, p.N, p.Npad, p.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

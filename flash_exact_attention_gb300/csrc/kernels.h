@@ -20,6 +20,50 @@ struct FwdParams {
   unsigned int* err;    // device error word
 };
 
+// Backward parameters of the main kernel (everything but the tensor maps).
+struct BwdParams {
+  void* dk;             // bf16 [B, Hkv, N, D]
+  void* dv;             // bf16 [B, Hkv, N, D]
+  float* dq_acc;        // fp32 [B*Hq, Npad, D], zeroed by bwd_preprocess
+  const float* lse2;    // fp32 [B*Hq, Npad]: LSE * log2(e); +inf for rows >= N
+  const float* delta;   // fp32 [B*Hq, Npad]: rowsum(dO * O); 0 for rows >= N
+  int B, Hq, Hkv, N;
+  int Npad;             // N rounded up to a multiple of 128
+  int G;                // Hq / Hkv
+  int num_kv_tiles;     // ceil(N / 128)
+  float scale;          // softmax scale
+  float scale_log2;     // scale * log2(e)
+  uint64_t timeout_ns;
+  unsigned int* err;
+};
+
+// Device pointers of the backward's fp32 scratch.
+struct BwdScratch {
+  float* dq_acc;
+  float* lse2;
+  float* delta;
+};
+
+// Bytes of fp32 scratch the backward needs for these sizes.
+size_t bwd_scratch_bytes(int B, int Hq, int N, int D);
+
+// Enqueues preprocess, main and postprocess kernels of the backward.
+cudaError_t launch_bwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdParams& p, const void* o,
+                           const void* dout, const float* lse, void* dq, bool causal,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, const void* o,
+                            const void* dout, const float* lse, void* dq, bool causal,
+                            cudaStream_t stream);
+
+// Host helpers shared by the entry points (attn_api.cu).
+int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale);
+int device_setup(int* dev_out, unsigned int** err_out);
+int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH);
+uint64_t wait_timeout_ns();
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 // Each launcher enqueues one forward kernel; returns the launch's cudaError_t.
 cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const FwdParams& p, bool causal, cudaStream_t stream);

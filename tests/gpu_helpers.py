@@ -75,5 +75,9 @@ def torch_index(rows):
 
 
 def rel_fro(g, ref):
+    """||g - ref||_F / ||ref||_F.  When the exact gradient is (near) zero -- e.g.
+    dQ and dK with a single key, where dS = 0 -- the denominator is floored at
+    an RMS of 1e-3 so that rounding noise is judged on an absolute scale."""
     g = np.asarray(g, dtype=np.float64)
-    return float(np.linalg.norm((g - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))
+    floor = 1e-3 * np.sqrt(max(ref.size, 1))
+    return float(np.linalg.norm((g - ref).ravel()) / max(np.linalg.norm(ref.ravel()), floor))
