@@ -5,7 +5,7 @@ in ``include/attn.h``).  This package only builds that library and marshals
 arguments to it; PyTorch supplies device memory and streams.  There is no CPU
 fallback: if the library is missing the calls raise.
 """
-__all__ = ["attn_fwd", "attn_bwd", "attn_status_string", "attn_device_status",
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_status_string", "attn_device_status",
            "flash_attn", "flash_attn_bwd", "AttnError"]
 
 

@@ -17,6 +17,7 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_DEVICE_TIMEOUT = 4
 ATTN_ERR_ARCH = 5
+ATTN_ERR_SCRATCH_LIMIT = 6
 
 _lib = None
 
@@ -25,6 +26,9 @@ _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "attn_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_bwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
+    "attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P],
+                         _I),
+    "attn_bwd_noalloc_scratch_limit": ([], ctypes.c_longlong),
     "attn_status_string": ([_I], ctypes.c_char_p),
     "attn_device_status": ([_P], _I),
     "attn_set_wait_timeout_ms": ([_I], _I),
@@ -89,6 +93,14 @@ def attn_bwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq,
     return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D,
                            int(bool(causal)), float(scale), _stream_handle(stream),
                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
+                     dv):
+    """Raw call of the backward that allocates nothing (fixed scratch array)."""
+    return load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N,
+                                   D, int(bool(causal)), float(scale), _stream_handle(stream),
+                                   _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
 
 
 def attn_status_string(status):

@@ -188,6 +188,8 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_CUDA: return "CUDA call or kernel launch failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case ATTN_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case ATTN_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than attn_bwd_noalloc's fixed array holds";
     default: return "unknown status";
   }
 }

@@ -12,8 +12,6 @@ size_t bwd_scratch_bytes(int B, int Hq, int N, int D) {
   return rows * (size_t)D * 4 + 2 * rows * 4;  // dQ accumulator, LSE2, Delta
 }
 
-namespace {
-
 BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D) {
   const size_t npad = ((size_t)N + 127) / 128 * 128;
   const size_t rows = (size_t)B * Hq * npad;
@@ -24,11 +22,9 @@ BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D) {
   return s;
 }
 
-}  // namespace
-
 // Validates everything that can be checked on the host; returns ATTN_OK and
 // fills *params (except scratch pointers) and the tensor maps.
-static int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
+int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, int B, int Hq, int Hkv, int N, int D, float scale,
                        const void* dout, void* dq, void* dk, void* dv, BwdParams* p,
                        CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo) {
@@ -63,7 +59,7 @@ static int bwd_prepare(const void* q, const void* k, const void* v, const void* 
   return ATTN_OK;
 }
 
-static int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
                       const float* lse, void* dq, int D, int causal, cudaStream_t s) {
   cudaError_t e = (D == 64) ? launch_bwd_d64(tq, tk, tv, tdo, p, o, dout, lse, dq, causal != 0, s)

@@ -47,6 +47,22 @@ struct BwdScratch {
 // Bytes of fp32 scratch the backward needs for these sizes.
 size_t bwd_scratch_bytes(int B, int Hq, int N, int D);
 
+// Splits one scratch block of bwd_scratch_bytes() into its three arrays.
+BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D);
+
+// Host-side validation and set-up of a backward call (tensor maps and every
+// parameter except the scratch pointers).  Returns ATTN_OK, an error code, or
+// -1 when there is nothing to compute.
+int bwd_prepare(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                int B, int Hq, int Hkv, int N, int D, float scale, const void* dout, void* dq,
+                void* dk, void* dv, BwdParams* p, CUtensorMap* tq, CUtensorMap* tk,
+                CUtensorMap* tv, CUtensorMap* tdo);
+
+// Enqueues the three backward kernels with the scratch already in `p`.
+int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
+               const float* lse, void* dq, int D, int causal, cudaStream_t s);
+
 // Enqueues preprocess, main and postprocess kernels of the backward.
 cudaError_t launch_bwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const BwdParams& p, const void* o,

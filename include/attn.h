@@ -61,7 +61,9 @@ enum attn_status_code {
   ATTN_ERR_UNSUPPORTED = 2,    /* head dim not in {64, 128} */
   ATTN_ERR_CUDA = 3,           /* a CUDA runtime/driver call or launch failed */
   ATTN_ERR_DEVICE_TIMEOUT = 4, /* a bounded device wait ran out (see attn_device_status) */
-  ATTN_ERR_ARCH = 5            /* the current device is not compute capability 10.3 */
+  ATTN_ERR_ARCH = 5,           /* the current device is not compute capability 10.3 */
+  ATTN_ERR_SCRATCH_LIMIT = 6   /* attn_bwd_noalloc: the problem needs more scratch than
+                                  its fixed array holds */
 };
 
 /*
@@ -85,6 +87,32 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
              float scale, void* stream, const void* dout, void* dq, void* dk,
              void* dv);
+
+/*
+ * Backward without any device allocation.  No counterpart in the paper: this
+ * is a deployment variant of attn_bwd for callers that cannot call the CUDA
+ * allocator -- a process whose device memory is owned by its own pool, or a
+ * serving loop that allows no allocation after start-up.
+ * Arguments, layouts, results and error codes are those of attn_bwd.  The fp32
+ * scratch lives in one fixed array in device memory of
+ * attn_bwd_noalloc_scratch_limit() bytes (32 MiB), which must hold
+ * B*Hq*roundup(N,128)*(D+2)*4 bytes; larger problems return
+ * ATTN_ERR_SCRATCH_LIMIT before any device work.
+ *   - Every call on a device shares that array.  Calls that can overlap on the
+ *     GPU (other streams, unordered host threads) race and give wrong results.
+ *   - The array keeps the previous call's contents; each call rewrites all it
+ *     reads before reading it.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it: make it before any stream capture.
+ *   - The array occupies device memory from the first call on a device until
+ *     the process exits.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                     float scale, void* stream, const void* dout, void* dq, void* dk, void* dv);
+
+/* Size in bytes of attn_bwd_noalloc's fixed scratch array. */
+long long attn_bwd_noalloc_scratch_limit(void);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char* attn_status_string(int status);

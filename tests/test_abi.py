@@ -17,7 +17,7 @@ def _declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+            names += re.findall(r"^[A-Za-z_][\w \t\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)
     return names
 
 
@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    for st in range(6):
+    for st in range(7):
         assert binding.status_text(st)
     assert binding.status_text(99) == "unknown status"
     assert binding.load().attn_version() >> 16 == 1
@@ -92,3 +92,14 @@ def test_no_device_reports_cuda_error_not_crash():
     lib = binding.load()
     st = lib.attn_fwd(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 4, 2, 128, 64, 0, 0.125, None)
     assert st in (binding.ATTN_ERR_CUDA, binding.ATTN_ERR_ARCH)
+
+
+def test_noalloc_backward_rejects_problems_beyond_its_fixed_scratch():
+    lib = binding.load()
+    limit = lib.attn_bwd_noalloc_scratch_limit()
+    assert limit == 32 << 20
+    # B=1, H=16, N=8192, D=128 needs 16*8192*130*4 bytes > 32 MiB
+    st = lib.attn_bwd_noalloc(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 16, 16, 8192, 128, 0,
+                              0.08, None, 0x6000, 0x7000, 0x8000, 0x9000)
+    assert st == binding.ATTN_ERR_SCRATCH_LIMIT
+    assert "scratch" in binding.status_text(st)
