@@ -112,9 +112,9 @@ __global__ void __launch_bounds__(320, 1)
 
   // ---- work unit: (query block of 256 rows, batch, query head)
   const int BH = p.B * p.Hq;
-  int qb = (int)blockIdx.x / BH;
-  if (CAUSAL) qb = p.num_qblocks - 1 - qb;  // longest rows first
-  const int bh = (int)blockIdx.x % BH;
+  const int qb = CAUSAL ? p.num_qblocks - 1 - (int)blockIdx.x / BH
+                        : (int)blockIdx.x % p.num_qblocks;
+  const int bh = CAUSAL ? (int)blockIdx.x % BH : (int)blockIdx.x / p.num_qblocks;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / p.G;
   const int q_row0 = qb * 256;
@@ -271,27 +271,37 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mp[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+      for (int c = 16; c < 128; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = fmax3(mp[k], s[c + k], s[c + 8 + k]);
+      const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]),
+                             fmaxf(mp[6], mp[7]));
       const float m_new = fmaxf(m_used, mx * C);
       const bool need = (m_new - m_used) > kRescaleThreshold;
       const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
       if (need) m_used = m_new;
       l *= corr;
-      const float neg_m = -m_used;
+      const float2 c2 = make_float2(C, C);
+      const float2 nm2 = make_float2(-m_used, -m_used);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
       uint32_t pk[64];
-      float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[c], C, neg_m));
-        const float p1 = ex2_approx(fmaf(s[c + 1], C, neg_m));
-        sum += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+        const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, nm2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pp);
+        pk[c / 2] = pack_bf16x2(pp.x, pp.y);
+        if (c == 62) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       }
-      l += sum;
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      l += a.x + a.y;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O_t is stable here: its last update was committed before S_t(j).
 #pragma unroll
