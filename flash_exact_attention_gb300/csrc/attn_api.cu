@@ -89,6 +89,20 @@ int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 3-D map over a contiguous fp32 [BH, rows, D] array: dims (D, rows, BH), box
+// (32, 128, 1) (128-byte rows), 128-byte swizzle.  Used for the dQ reduce-add.
+int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)rows * D * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // Shape / scale checks shared by the forward and backward.
 int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale) {
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ATTN_ERR_INVALID_ARG;

@@ -19,12 +19,14 @@
 //                     dK_j += dS^T Q_i            (A = dS^T from shared memory)
 //                     dQ_i  = dS K_j              (A = the same dS^T tile read MN-major)
 //                   dK/dV stay in TMEM across the whole group (no GQA reduction
-//                   pass); dQ_i is added to the fp32 accumulator with vector
-//                   reductions by a dedicated warpgroup.
+//                   pass).  dQ_i goes TMEM -> registers -> the Q_i/dO_i ring
+//                   stage (dead once the dQ MMA has finished) -> TMA tensor
+//                   reduce-add into the fp32 accumulator; only then is the stage
+//                   handed back to the producer.
 //   bwd_postprocess dQ = scale * dQacc -> bf16.
 //
 // Warp roles of bwd_kernel (10 warps): 0-3 dS (one thread per key row) and the
-// dK/dV epilogue; 4-7 dQ reduction (one thread per query row); 8 TMA producer
+// dK/dV epilogue; 4-7 dQ staging and reduction (one thread per query row); 8 TMA producer
 // (K_j, V_j once; Q_i, dO_i, LSE2, Delta per iteration into a 2-stage ring);
 // 9 TMEM allocator and MMA issuer.
 //
@@ -51,8 +53,8 @@ struct BwdCfg {
   static constexpr int kdS = 6 * kTile;      // dS^T tile: 128 keys x 128 queries bf16
   static constexpr int kVec = kdS + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
   static constexpr int kBar = kVec + 2 * 1024;
-  // kv_full, qd_full[2], qd_empty[2], s_ready, ds_ready, dq_ready, dq_free, all_done
-  static constexpr int kNumBars = 10;
+  // kv_full, qd_full[2], qd_empty[2], s_ready, ds_ready, dq_ready, dq_free, all_done, staged
+  static constexpr int kNumBars = 11;
   static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
@@ -62,7 +64,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using Cfg = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bar_dq = bar0 + 8u * 7;
   const uint32_t bar_dq_free = bar0 + 8u * 8;
   const uint32_t bar_done = bar0 + 8u * 9;
+  const uint32_t bar_staged = bar0 + 8u * 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -98,6 +101,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dq, 1);
     mbar_init(bar_dq_free, 4);
     mbar_init(bar_done, 1);
+    mbar_init(bar_staged, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -207,8 +212,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = mbar_wait(bar_ds, (uint32_t)it & 1u, wc))) break;
         tc_fence_after();
         issue_grads(s, it > 0);
-        mma_commit(bar_dq);
-        mma_commit(bar_qd_empty(s));
+        mma_commit(bar_dq);  // the dQ warps release stage s after staging dQ in it
         if (it + 1 < n_it) {
           const int s1 = (it + 1) & 1;
           if (!(ok = mbar_wait(bar_qd_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
@@ -224,12 +228,17 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) mbar_wait_drain(bar_done, 0, wc);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ dQ reduction
+    // ------------------------------------------------------------ dQ staging + reduce-add
     const int wq = warp & 3;
     const int row = wq * 32 + lane;  // query row within the tile
     const uint32_t tq = tdP + ((uint32_t)(wq * 32) << 16);
+    const bool issuer = (warp == 4 && lane == 0);
+    const uint32_t swz = (uint32_t)(row & 7);
+    bool ok = true;  // per thread; folded into the warp-uniform check below
     for (int it = 0; it < n_it; ++it) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, (uint32_t)it & 1u, wc))) break;
+      const int s = it & 1;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_dq, (uint32_t)it & 1u, wc));
+      if (!ok) break;
       tc_fence_after();
       uint32_t r[D / 32][32];
 #pragma unroll
@@ -238,16 +247,32 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_free);
-      // Rows past N belong to the padded accumulator and receive zeros.
-      float* dst = p.dq_acc + ((size_t)q_head(it) * p.Npad + (size_t)q_tile(it) * 128 + row) * D;
+      // Stage (all MMAs reading it have completed): D/32 boxes of [128 rows x
+      // 32 fp32], 128-byte rows, 16-byte chunks swizzled by row & 7.
+      const uint32_t stage = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile + (uint32_t)row * 128u;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c)
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          red_add_v4(dst + c * 32 + v * 4, __uint_as_float(r[c][4 * v]),
-                     __uint_as_float(r[c][4 * v + 1]), __uint_as_float(r[c][4 * v + 2]),
-                     __uint_as_float(r[c][4 * v + 3]));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           stage + c * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
+                       "r"(r[c][4 * v]), "r"(r[c][4 * v + 1]), "r"(r[c][4 * v + 2]),
+                       "r"(r[c][4 * v + 3])
+                       : "memory");
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_staged);
+      if (issuer && (ok = mbar_wait(bar_staged, (uint32_t)it & 1u, wc))) {
+        const uint32_t base = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tma_reduce_add_3d(&tm_dq, base + c * Cfg::kBox, c * 32, q_tile(it) * 128, q_head(it));
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(bar_qd_empty(s));
+      }
     }
+    if (issuer) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ dS = P o (dP - Delta)
     const int row = warp * 32 + lane;  // key row within the tile
@@ -267,37 +292,53 @@ __global__ void __launch_bounds__(320, 1)
       const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kVec + s * 1024);
       const float* delta = lse2 + 128;
       const bool diag = CAUSAL && q_tile(it) == j;
+      const float2 c2 = make_float2(C, C);
+      // 16 query columns per chunk; the loads of chunk c+1 are in flight while
+      // chunk c is computed.
+      uint32_t sr[2][16], dr[2][16];
+      tmem_ld16(tS + lane_off, sr[0]);
+      tmem_ld16(tdP + lane_off, dr[0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 query columns at a time
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + lane_off + c * 32, sr);
-        tmem_ld32(tdP + lane_off + c * 32, dr);
+      for (int c = 0; c < 8; ++c) {
+        const int b = c & 1;
         tmem_ld_wait();
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int qc = c * 32 + e;
-          const float2 l2 = *reinterpret_cast<const float2*>(lse2 + qc);
-          const float2 dl = *reinterpret_cast<const float2*>(delta + qc);
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), C, -l2.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), C, -l2.y));
-          if (diag) {  // causal: query < key is masked
-            if (qc < row) p0 = 0.f;
-            if (qc + 1 < row) p1 = 0.f;
-          }
-          if (!key_live) p0 = p1 = 0.f;
-          const float d0 = p0 * (__uint_as_float(dr[e]) - dl.x);
-          const float d1 = p1 * (__uint_as_float(dr[e + 1]) - dl.y);
-          pk[e / 2] = pack_bf16x2(p0, p1);
-          dk[e / 2] = pack_bf16x2(d0, d1);
+        if (c + 1 < 8) {
+          tmem_ld16(tS + lane_off + (c + 1) * 16, sr[b ^ 1]);
+          tmem_ld16(tdP + lane_off + (c + 1) * 16, dr[b ^ 1]);
         }
-        // P^T (bf16) over S^T columns already read: chunk c fills columns [16c, 16c+16).
-        tmem_st16(tS + lane_off + c * 16, pk);
-        // dS^T row to shared memory in the 128-byte swizzled layout.
-        const uint32_t box = ds_row + (uint32_t)(c >> 1) * Cfg::kBox;
+        uint32_t pk[8], dk[8];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint32_t chunk = ((uint32_t)((c & 1) * 4 + v)) ^ swz;
+        for (int e = 0; e < 16; e += 4) {
+          const int qc = c * 16 + e;
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + qc);
+          const float4 d4 = *reinterpret_cast<const float4*>(delta + qc);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int ee = e + 2 * h;
+            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(sr[b][ee]), __uint_as_float(sr[b][ee + 1])), c2, nl);
+            float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (diag) {  // causal: query < key is masked
+              if (qc + 2 * h < row) pp.x = 0.f;
+              if (qc + 2 * h + 1 < row) pp.y = 0.f;
+            }
+            if (!key_live) pp = make_float2(0.f, 0.f);
+            const float2 dd = __fadd2_rn(
+                make_float2(__uint_as_float(dr[b][ee]), __uint_as_float(dr[b][ee + 1])), nd);
+            const float2 ds = __fmul2_rn(pp, dd);
+            pk[ee / 2] = pack_bf16x2(pp.x, pp.y);
+            dk[ee / 2] = pack_bf16x2(ds.x, ds.y);
+          }
+        }
+        // P^T (bf16) over S^T columns already read: chunk c fills columns [8c, 8c+8).
+        tmem_st8(tS + lane_off + c * 8, pk);
+        // dS^T row to shared memory in the 128-byte swizzled layout.
+        const uint32_t box = ds_row + (uint32_t)(c >> 2) * Cfg::kBox;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const uint32_t chunk = ((uint32_t)((c & 3) * 2 + v)) ^ swz;
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + chunk * 16),
                        "r"(dk[4 * v]), "r"(dk[4 * v + 1]), "r"(dk[4 * v + 2]), "r"(dk[4 * v + 3])
                        : "memory");

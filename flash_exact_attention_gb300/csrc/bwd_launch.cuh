@@ -9,6 +9,8 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const BwdParams& p, const void* o,
                             const void* dout, const float* lse, void* dq, cudaStream_t stream) {
   using Cfg = BwdCfg<D>;
+  CUtensorMap tdq;  // the fp32 dQ accumulator, target of the TMA reduce-add
+  if (encode_f32_rows_map(&tdq, p.dq_acc, D, p.Npad, p.B * p.Hq) != 0) return cudaErrorInvalidValue;
   const long long prow = (long long)p.B * p.Hq * p.Npad;  // padded rows
   bwd_preprocess<D><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse,
@@ -19,7 +21,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long orow = (long long)p.B * p.Hq * p.N;

@@ -77,6 +77,7 @@ cudaError_t launch_bwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
 int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale);
 int device_setup(int* dev_out, unsigned int** err_out);
 int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH);
+int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH);
 uint64_t wait_timeout_ns();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
