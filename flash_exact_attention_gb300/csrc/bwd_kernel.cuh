@@ -21,17 +21,24 @@
 //                   dK/dV stay in TMEM across the whole group (no GQA reduction
 //                   pass).  dQ_i goes TMEM -> registers -> the Q_i/dO_i ring
 //                   stage (dead once the dQ MMA has finished) -> TMA tensor
-//                   reduce-add into the fp32 accumulator; only then is the stage
-//                   handed back to the producer.
+//                   reduce-add into the fp32 accumulator, issued by the producer
+//                   thread, which reloads the stage as soon as the reduce-add has
+//                   read it.
 //   bwd_postprocess dQ = scale * dQacc -> bf16.
 //
-// Warp roles of bwd_kernel (10 warps): 0-3 dS (one thread per key row) and the
-// dK/dV epilogue; 4-7 dQ staging and reduction (one thread per query row); 8 TMA producer
-// (K_j, V_j once; Q_i, dO_i, LSE2, Delta per iteration into a 2-stage ring);
-// 9 TMEM allocator and MMA issuer.
+// Warp roles of bwd_kernel (10 warps):
+//   0-7  compute warps.  Warp w covers TMEM lanes 32*(w%4).. and column half
+//        w/4: it computes dS for 64 of the 128 queries of its 32 key rows, then
+//        stages half of the dQ columns of its 32 query rows, and at the end
+//        writes dV (half 0) or dK (half 1) of its key rows.
+//   8    TMA producer (K_j, V_j once; Q_i, dO_i, LSE2, Delta per iteration into a
+//        2-stage ring) and issuer of the dQ reduce-adds.
+//   9    TMEM allocator and MMA issuer.
 //
-// TMEM columns: [0,128) S^T, with P^T (bf16) written over its first 64;
-// [128,256) dP^T, later overwritten by dQ_i; [256,256+D) dV; [256+D,256+2D) dK.
+// TMEM columns: [0,128) S^T, with P^T (bf16) of queries 0-63 written over
+// columns [0,32) and of queries 64-127 over [64,96) (each half stays inside the
+// S^T columns its own warps read); [128,256) dP^T, later overwritten by dQ_i;
+// [256,256+D) dV; [256+D,256+2D) dK.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -53,7 +60,7 @@ struct BwdCfg {
   static constexpr int kdS = 6 * kTile;      // dS^T tile: 128 keys x 128 queries bf16
   static constexpr int kVec = kdS + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
   static constexpr int kBar = kVec + 2 * 1024;
-  // kv_full, qd_full[2], qd_empty[2], s_ready, ds_ready, dq_ready, dq_free, all_done, staged
+  // kv_full, qd_full[2], staged[2], s_ready, ds_ready, dq_ready, dq_free, all_done, red_go
   static constexpr int kNumBars = 11;
   static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
   static constexpr int kThreads = 320;
@@ -80,13 +87,15 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bar0 = sbase + Cfg::kBar;
   const uint32_t bar_kv = bar0;
   auto bar_qd_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_qd_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto bar_staged = [&](int h) { return bar0 + 8u * (3 + h); };  // dQ column half h staged
   const uint32_t bar_s = bar0 + 8u * 5;
   const uint32_t bar_ds = bar0 + 8u * 6;
   const uint32_t bar_dq = bar0 + 8u * 7;
   const uint32_t bar_dq_free = bar0 + 8u * 8;
   const uint32_t bar_done = bar0 + 8u * 9;
-  const uint32_t bar_staged = bar0 + 8u * 10;
+  // The producer has taken step it's staged dQ: the compute warps may signal
+  // the next step's staging (keeps staged[] from running a phase ahead).
+  const uint32_t bar_red_go = bar0 + 8u * 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -94,14 +103,14 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_qd_full(s), 1);
-      mbar_init(bar_qd_empty(s), 1);
+      mbar_init(bar_staged(s), 4);
     }
     mbar_init(bar_s, 1);
-    mbar_init(bar_ds, 4);
+    mbar_init(bar_ds, 8);
     mbar_init(bar_dq, 1);
-    mbar_init(bar_dq_free, 4);
+    mbar_init(bar_dq_free, 8);
     mbar_init(bar_done, 1);
-    mbar_init(bar_staged, 4);
+    mbar_init(bar_red_go, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -134,18 +143,15 @@ __global__ void __launch_bounds__(320, 1)
                  tdK = tmem_base + 256 + D;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer + dQ reduce
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_kv, 2 * Cfg::kTile);
       for (int c = 0; c < Cfg::kBoxes; ++c) {
         tma_load_3d(sbase + Cfg::kK + c * Cfg::kBox, &tm_k, bar_kv, c * 64, j * 128, bhkv);
         tma_load_3d(sbase + Cfg::kV + c * Cfg::kBox, &tm_v, bar_kv, c * 64, j * 128, bhkv);
       }
-      int it = 0;
-      bool ok = true;
-      for (; it < n_it; ++it) {
+      auto load_stage = [&](int it) {
         const int s = it & 1;
-        if (!(ok = mbar_wait(bar_qd_empty(s), ((uint32_t)(it >> 1) & 1u) ^ 1u, wc))) break;
         const int bhq = q_head(it), i = q_tile(it);
         const uint32_t qs = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
         mbar_arrive_expect_tx(bar_qd_full(s), 2 * Cfg::kTile + 1024);
@@ -157,9 +163,32 @@ __global__ void __launch_bounds__(320, 1)
         const size_t voff = (size_t)bhq * p.Npad + (size_t)i * 128;
         bulk_load(sbase + Cfg::kVec + s * 1024, p.lse2 + voff, 512, bar_qd_full(s));
         bulk_load(sbase + Cfg::kVec + s * 1024 + 512, p.delta + voff, 512, bar_qd_full(s));
+      };
+      int loaded = 0;
+      for (; loaded < 2 && loaded < n_it; ++loaded) load_stage(loaded);
+      bool ok = true;
+      for (int it = 0; it < n_it && ok; ++it) {
+        // dQ_it was staged in stage it&1 (its MMAs are all complete by then):
+        // add it to the accumulator half by half, then reuse the stage.
+        const uint32_t stage = sbase + Cfg::kQ0 + (it & 1) * 2 * Cfg::kTile;
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait(bar_staged(h), (uint32_t)it & 1u, wc))) break;
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) {
+            const int c = h * (D / 64) + cc;  // 32-column box
+            tma_reduce_add_3d(&tm_dq, stage + c * Cfg::kBox, c * 32, q_tile(it) * 128,
+                              q_head(it));
+          }
+        }
+        bulk_commit();
+        if (ok) mbar_arrive(bar_red_go);
+        bulk_wait_read_all();
+        if (ok && loaded < n_it) load_stage(loaded++);
       }
+      bulk_wait_all();
       if (!ok) {
-        for (int f = (it > 2 ? it - 2 : 0); f < it; ++f)
+        // Let every load already issued land before the CTA can exit.
+        for (int f = (loaded > 2 ? loaded - 2 : 0); f < loaded; ++f)
           mbar_wait_drain(bar_qd_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
         mbar_wait_drain(bar_kv, 0, wc);
       }
@@ -185,8 +214,9 @@ __global__ void __launch_bounds__(320, 1)
       auto issue_grads = [&](int s, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO  (K = 128 queries)
-          mma_ts(tdV, tS + kk * 8, make_sdesc_sw128(do_addr(s) + kk * 2048, Cfg::kBox, 1024),
-                 kIdescB_MN, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tdV, tS + (kk / 4) * 64 + (kk % 4) * 8,
+                 make_sdesc_sw128(do_addr(s) + kk * 2048, Cfg::kBox, 1024), kIdescB_MN,
+                 (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q  (K = 128 queries)
           const uint32_t off = (kk / 4) * Cfg::kBox + (kk % 4) * 32;
@@ -227,89 +257,46 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(bar_done);
       if (!ok) mbar_wait_drain(bar_done, 0, wc);
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ dQ staging + reduce-add
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;  // query row within the tile
-    const uint32_t tq = tdP + ((uint32_t)(wq * 32) << 16);
-    const bool issuer = (warp == 4 && lane == 0);
-    const uint32_t swz = (uint32_t)(row & 7);
-    bool ok = true;  // per thread; folded into the warp-uniform check below
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1;
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_dq, (uint32_t)it & 1u, wc));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t r[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tq + c * 32, r[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dq_free);
-      // Stage (all MMAs reading it have completed): D/32 boxes of [128 rows x
-      // 32 fp32], 128-byte rows, 16-byte chunks swizzled by row & 7.
-      const uint32_t stage = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile + (uint32_t)row * 128u;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           stage + c * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
-                       "r"(r[c][4 * v]), "r"(r[c][4 * v + 1]), "r"(r[c][4 * v + 2]),
-                       "r"(r[c][4 * v + 3])
-                       : "memory");
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_staged);
-      if (issuer && (ok = mbar_wait(bar_staged, (uint32_t)it & 1u, wc))) {
-        const uint32_t base = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-          tma_reduce_add_3d(&tm_dq, base + c * Cfg::kBox, c * 32, q_tile(it) * 128, q_head(it));
-        bulk_commit();
-        bulk_wait_read_all();
-        mbar_arrive(bar_qd_empty(s));
-      }
-    }
-    if (issuer) bulk_wait_all();
   } else {
-    // ------------------------------------------------------------ dS = P o (dP - Delta)
-    const int row = warp * 32 + lane;  // key row within the tile
+    // ------------------------------------------------------------ compute warps 0-7
+    const int wq = warp & 3;   // TMEM lane quadrant
+    const int ch = warp >> 2;  // column half
+    const int row = wq * 32 + lane;  // key row (dS, epilogue) / query row (dQ staging)
     const int kj = j * 128 + row;
     const bool key_live = kj < p.N;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float C = p.scale_log2;
-    const uint32_t ds_row = sbase + Cfg::kdS + (uint32_t)row * 128u;
+    const float2 c2 = make_float2(C, C);
     const uint32_t swz = (uint32_t)(row & 7);
+    const uint32_t ds_row = sbase + Cfg::kdS + (uint32_t)ch * Cfg::kBox + (uint32_t)row * 128u;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
+      // ---- dS = P o (dP - Delta) for queries [64ch, 64ch + 64) of this key row
       ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)it & 1u, wc) &&
                                        mbar_wait(bar_qd_full(s), (uint32_t)(it >> 1) & 1u, wc));
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kVec + s * 1024);
+      const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kVec + s * 1024) + ch * 64;
       const float* delta = lse2 + 128;
       const bool diag = CAUSAL && q_tile(it) == j;
-      const float2 c2 = make_float2(C, C);
-      // 16 query columns per chunk; the loads of chunk c+1 are in flight while
-      // chunk c is computed.
+      const uint32_t ts = tS + lane_off + (uint32_t)ch * 64u;
+      const uint32_t tp = tdP + lane_off + (uint32_t)ch * 64u;
       uint32_t sr[2][16], dr[2][16];
-      tmem_ld16(tS + lane_off, sr[0]);
-      tmem_ld16(tdP + lane_off, dr[0]);
+      tmem_ld16(ts, sr[0]);
+      tmem_ld16(tp, dr[0]);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int b = c & 1;
+      for (int c = 0; c < 4; ++c) {  // 16 query columns per chunk, the next one in flight
+        const int bb = c & 1;
         tmem_ld_wait();
-        if (c + 1 < 8) {
-          tmem_ld16(tS + lane_off + (c + 1) * 16, sr[b ^ 1]);
-          tmem_ld16(tdP + lane_off + (c + 1) * 16, dr[b ^ 1]);
+        if (c + 1 < 4) {
+          tmem_ld16(ts + (c + 1) * 16, sr[bb ^ 1]);
+          tmem_ld16(tp + (c + 1) * 16, dr[bb ^ 1]);
         }
         uint32_t pk[8], dk[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
-          const int qc = c * 16 + e;
+          const int qc = c * 16 + e;  // query within this half
           const float4 l4 = *reinterpret_cast<const float4*>(lse2 + qc);
           const float4 d4 = *reinterpret_cast<const float4*>(delta + qc);
 #pragma unroll
@@ -318,28 +305,28 @@ __global__ void __launch_bounds__(320, 1)
             const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
             const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
             const float2 x = __ffma2_rn(
-                make_float2(__uint_as_float(sr[b][ee]), __uint_as_float(sr[b][ee + 1])), c2, nl);
+                make_float2(__uint_as_float(sr[bb][ee]), __uint_as_float(sr[bb][ee + 1])), c2, nl);
             float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             if (diag) {  // causal: query < key is masked
-              if (qc + 2 * h < row) pp.x = 0.f;
-              if (qc + 2 * h + 1 < row) pp.y = 0.f;
+              const int q = ch * 64 + qc + 2 * h;
+              if (q < row) pp.x = 0.f;
+              if (q + 1 < row) pp.y = 0.f;
             }
             if (!key_live) pp = make_float2(0.f, 0.f);
             const float2 dd = __fadd2_rn(
-                make_float2(__uint_as_float(dr[b][ee]), __uint_as_float(dr[b][ee + 1])), nd);
+                make_float2(__uint_as_float(dr[bb][ee]), __uint_as_float(dr[bb][ee + 1])), nd);
             const float2 ds = __fmul2_rn(pp, dd);
             pk[ee / 2] = pack_bf16x2(pp.x, pp.y);
             dk[ee / 2] = pack_bf16x2(ds.x, ds.y);
           }
         }
-        // P^T (bf16) over S^T columns already read: chunk c fills columns [8c, 8c+8).
-        tmem_st8(tS + lane_off + c * 8, pk);
-        // dS^T row to shared memory in the 128-byte swizzled layout.
-        const uint32_t box = ds_row + (uint32_t)(c >> 2) * Cfg::kBox;
+        // P^T (bf16) over S^T columns this warp has already read.
+        tmem_st8(ts + c * 8, pk);
+        // dS^T row to shared memory (box ch) in the 128-byte swizzled layout.
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
-          const uint32_t chunk = ((uint32_t)((c & 3) * 2 + v)) ^ swz;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + chunk * 16),
+          const uint32_t chunk = ((uint32_t)(c * 2 + v)) ^ swz;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ds_row + chunk * 16),
                        "r"(dk[4 * v]), "r"(dk[4 * v + 1]), "r"(dk[4 * v + 2]), "r"(dk[4 * v + 3])
                        : "memory");
         }
@@ -349,33 +336,59 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
+
+      // ---- dQ_it: TMEM -> registers -> stage `s` (all MMAs reading it are done)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, (uint32_t)it & 1u, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[D / 64][32];  // this warp's D/2 dQ columns of its query row
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(tdP + lane_off + (ch * (D / 64) + cc) * 32, r[cc]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_free);
+      // Boxes of [128 rows x 32 fp32], 128-byte rows, 16-byte chunks swizzled by row & 7.
+      const uint32_t stage = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile + (uint32_t)row * 128u;
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc)
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           stage + (ch * (D / 64) + cc) * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
+                       "r"(r[cc][4 * v]), "r"(r[cc][4 * v + 1]), "r"(r[cc][4 * v + 2]),
+                       "r"(r[cc][4 * v + 3])
+                       : "memory");
+      fence_proxy_async_smem();
+      if (it > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_red_go, (uint32_t)(it - 1) & 1u, wc));
+        if (!ok) break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_staged(ch));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, wc));
     if (ok) {
+      // Epilogue: half 0 writes dV, half 1 writes dK (scaled) of this key row.
       tc_fence_after();
       const size_t orow = ((size_t)bhkv * p.N + (size_t)(key_live ? kj : 0)) * D;
-      uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + orow);
-      uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + orow);
+      uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ch ? p.dk : p.dv) + orow);
+      const float mul = ch ? p.scale : 1.f;
+      const uint32_t src = (ch ? tdK : tdV) + lane_off;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const float mul = which ? p.scale : 1.f;
-        uint4* out = which ? dk : dv;
-        const uint32_t src = (which ? tdK : tdV) + lane_off;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(src + c * 32, rr);
+        tmem_ld_wait();
+        if (key_live) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(src + c * 32, r);
-          tmem_ld_wait();
-          if (key_live) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * mul, __uint_as_float(r[8 * v + 1]) * mul);
-              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * mul, __uint_as_float(r[8 * v + 3]) * mul);
-              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * mul, __uint_as_float(r[8 * v + 5]) * mul);
-              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * mul, __uint_as_float(r[8 * v + 7]) * mul);
-              out[c * 4 + v] = w;
-            }
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(rr[8 * v + 0]) * mul, __uint_as_float(rr[8 * v + 1]) * mul);
+            w.y = pack_bf16x2(__uint_as_float(rr[8 * v + 2]) * mul, __uint_as_float(rr[8 * v + 3]) * mul);
+            w.z = pack_bf16x2(__uint_as_float(rr[8 * v + 4]) * mul, __uint_as_float(rr[8 * v + 5]) * mul);
+            w.w = pack_bf16x2(__uint_as_float(rr[8 * v + 6]) * mul, __uint_as_float(rr[8 * v + 7]) * mul);
+            out[c * 4 + v] = w;
           }
         }
       }
