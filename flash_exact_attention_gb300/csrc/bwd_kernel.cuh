@@ -127,12 +127,15 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // ---- work unit: (key tile j, batch, kv head); heaviest key tiles first when causal
-  const int BHkv = p.B * p.Hkv;
-  const int j = (int)blockIdx.x / BHkv;
-  const int bhkv = (int)blockIdx.x % BHkv;
-  const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
+  // ---- work unit: (key tile j, batch, kv head).  Non-causal: the key tiles of
+  // one head are consecutive, so the CTAs resident at one time share a few
+  // heads' Q, dO and dQ accumulator in L2.  Causal: the heaviest key tiles
+  // (smallest j) of all heads go first, for load balance.
   const int T = p.num_kv_tiles;
+  const int BHkv = p.B * p.Hkv;
+  const int j = CAUSAL ? (int)blockIdx.x / BHkv : (int)blockIdx.x % T;
+  const int bhkv = CAUSAL ? (int)blockIdx.x % BHkv : (int)blockIdx.x / T;
+  const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
   const int i0 = CAUSAL ? j : 0;
   const int n_i = T - i0;
   const int n_it = p.G * n_i;
