@@ -32,6 +32,7 @@ std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
 unsigned int* g_err_ptr[kMaxDevices] = {};
 int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 wrong arch
+int g_num_sms[kMaxDevices] = {};
 uint64_t g_timeout_ns = 2000ull * 1000ull * 1000ull;
 
 }  // namespace
@@ -53,6 +54,10 @@ int device_setup(int* dev_out, unsigned int** err_out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
     g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_num_sms[dev] = sms;
   }
   if (g_arch_ok[dev] < 0) return ATTN_ERR_ARCH;
   if (!g_err_ptr[dev]) {
@@ -72,6 +77,11 @@ int device_setup(int* dev_out, unsigned int** err_out) {
   *dev_out = dev;
   *err_out = g_err_ptr[dev];
   return ATTN_OK;
+}
+
+int device_sm_count(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return (dev >= 0 && dev < kMaxDevices) ? g_num_sms[dev] : 0;
 }
 
 // 3-D map over a contiguous bf16 [BH, N, D] tensor: dims (D, N, BH), box
@@ -145,7 +155,10 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.Hkv = Hkv;
   p.N = N;
   p.G = Hq / Hkv;
-  p.num_qblocks = (N + 255) / 256;
+  p.num_qblocks = ((N + 127) / 128 + 1) / 2;
+  // A causal grid that does not fill the GPU once is bounded by its longest
+  // CTA; pairing tile t with tile T-1-t shortens it (see fwd_kernel.cuh).
+  p.zigzag = (causal != 0) && (long long)p.num_qblocks * B * Hq < device_sm_count(dev);
   p.num_kv_tiles = (N + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();

@@ -110,18 +110,28 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // ---- work unit: (query block of 256 rows, batch, query head)
+  // ---- work unit: two 128-row query tiles t0 < t1 of one (batch, head).
+  //  * Non-causal: adjacent tiles (2qb, 2qb+1); the CTAs of one head are
+  //    consecutive so that those resident at one time share its K/V in L2.
+  //  * Causal, grid of at least one wave: adjacent tiles, longest blocks of all
+  //    heads first (both tiles are active in almost every step, so the MMAs of
+  //    one overlap the softmax of the other).
+  //  * Causal, grid smaller than one wave (p.zigzag): tiles qb and T-1-qb, so
+  //    every CTA runs T+1 tile steps; the longest CTA no longer carries two
+  //    full-length tiles, which is what bounds a grid that fits in one wave.
+  const int T = p.num_kv_tiles;
   const int BH = p.B * p.Hq;
-  const int qb = CAUSAL ? p.num_qblocks - 1 - (int)blockIdx.x / BH
-                        : (int)blockIdx.x % p.num_qblocks;
-  const int bh = CAUSAL ? (int)blockIdx.x % BH : (int)blockIdx.x / p.num_qblocks;
+  const bool zz = CAUSAL && p.zigzag;
+  const int qb = (CAUSAL && !zz) ? p.num_qblocks - 1 - (int)blockIdx.x / BH
+                                 : (int)blockIdx.x % p.num_qblocks;
+  const int bh = (CAUSAL && !zz) ? (int)blockIdx.x % BH : (int)blockIdx.x / p.num_qblocks;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / p.G;
-  const int q_row0 = qb * 256;
-  const bool has_t1 = q_row0 + 128 < p.N;
-  const int T = p.num_kv_tiles;
-  const int n0 = CAUSAL ? min(2 * qb + 1, T) : T;
-  const int n1 = has_t1 ? (CAUSAL ? min(2 * qb + 2, T) : T) : 0;
+  const int t0 = zz ? qb : 2 * qb;
+  const int t1 = zz ? T - 1 - qb : 2 * qb + 1;
+  const bool has_t1 = zz ? (t1 > t0) : (t1 * 128 < p.N);
+  const int n0 = CAUSAL ? t0 + 1 : T;
+  const int n1 = has_t1 ? (CAUSAL ? t1 + 1 : T) : 0;
   const int nkv = max(n0, n1);
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
 
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < nq; ++t)
         for (int c = 0; c < Cfg::kBoxes; ++c)
           tma_load_3d(sbase + Cfg::kQOff + t * Cfg::kTileBytes + c * Cfg::kBoxBytes, &tm_q, bar_q(),
-                      c * 64, q_row0 + t * 128, bh);
+                      c * 64, (t ? t1 : t0) * 128, bh);
       uint32_t it = 0;
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
@@ -239,8 +249,8 @@ __global__ void __launch_bounds__(320, 1)
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const int n_t = t ? n1 : n0;
-    const int qtile = 2 * qb + t;
-    const int grow = q_row0 + t * 128 + row;
+    const int qtile = t ? t1 : t0;
+    const int grow = qtile * 128 + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem_base + lane_off + 256u + (uint32_t)(t * 128);

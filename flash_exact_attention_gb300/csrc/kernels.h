@@ -13,7 +13,8 @@ struct FwdParams {
   float* lse;           // fp32 [B, Hq, N]
   int B, Hq, Hkv, N;
   int G;                // Hq / Hkv
-  int num_qblocks;      // ceil(N / 256): CTAs per (batch, head)
+  int num_qblocks;      // ceil(ceil(N / 128) / 2): CTAs per (batch, head)
+  int zigzag;           // causal only: pair query tiles t and T-1-t (see fwd_kernel.cuh)
   int num_kv_tiles;     // ceil(N / 128)
   float scale_log2;     // scale * log2(e)
   uint64_t timeout_ns;  // limit of every device-side wait
@@ -76,6 +77,7 @@ cudaError_t launch_bwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
 // Host helpers shared by the entry points (attn_api.cu).
 int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale);
 int device_setup(int* dev_out, unsigned int** err_out);
+int device_sm_count(int dev);
 int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH);
 int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH);
 uint64_t wait_timeout_ns();
