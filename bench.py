@@ -149,6 +149,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings: the slowest rank sets the job time."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(world_size, flops_per_rank_step, ms_per_step):
+    """Whole-job throughput: every rank does one step of the same size (weak scaling)."""
+    return world_size * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
+def rank_seed(seed, rank):
+    """Each rank draws its own batch: the replicas share no data and no collective."""
+    return seed + rank
+
+
 def _dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -173,7 +193,7 @@ def run_native(args):
     scale = scale_for(D)
     has_bwd = STEP_INCLUDES_BWD
 
-    x = make_inputs(B, Hq, Hkv, N, D, seed=args.seed + rank, with_do=True)
+    x = make_inputs(B, Hq, Hkv, N, D, seed=rank_seed(args.seed, rank), with_do=True)
     host = {n: to_torch_bf16(a).pin_memory() for n, a in x.items()}
     dev = {n: t.to("cuda") for n, t in host.items()}
     q, k, v, do = dev["q"], dev["k"], dev["v"], dev["do"]
@@ -254,11 +274,9 @@ def run_native(args):
     ms_step = ms_total / args.steps
     ms_fwd_launch = ms_fwd / args.steps
     ms_bwd_call = ms_bwd / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step, ms_fwd_launch, ms_bwd_call], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd_launch, ms_bwd_call = float(t[0]), float(t[1]), float(t[2])
-    value = ws * step_flops / (ms_step * 1e-3) / 1e12
+    ms_step, ms_fwd_launch, ms_bwd_call = max_over_ranks(
+        [ms_step, ms_fwd_launch, ms_bwd_call], dist, "cuda")
+    value = job_tflops(ws, step_flops, ms_step)
     fwd_tflops = ff / (ms_fwd_launch * 1e-3) / 1e12
     bwd_tflops = 2.5 * ff / (ms_bwd_call * 1e-3) / 1e12 if has_bwd else None
 
@@ -284,11 +302,8 @@ def run_native(args):
     g1.record(stream)
     barrier()
     ms_e2e = g0.elapsed_time(g1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t[0])
-    e2e_value = ws * step_flops / (ms_e2e * 1e-3) / 1e12
+    ms_e2e = max_over_ranks([ms_e2e], dist, "cuda")[0]
+    e2e_value = job_tflops(ws, step_flops, ms_e2e)
 
     peak_burst, peak_sust, peak_src = _measured_peaks()
     peak_note = ("%s bf16 burst (MEASURED_PEAKS.json)" % peak_src if peak_src == "measured"

@@ -32,6 +32,7 @@ SIGNATURES = {
     "attn_status_string": ([_I], ctypes.c_char_p),
     "attn_device_status": ([_P], _I),
     "attn_set_wait_timeout_ms": ([_I], _I),
+    "attn_selftest_wait_timeout": ([_I, _P], _I),
     "attn_version": ([], _I),
 }
 
@@ -109,6 +110,11 @@ def attn_status_string(status):
 
 def attn_device_status(stream=None):
     return load().attn_device_status(_stream_handle(stream))
+
+
+def attn_selftest_wait_timeout(timeout_ms, stream=None):
+    """Enqueues a kernel whose bounded wait is made to run out (diagnostic)."""
+    return load().attn_selftest_wait_timeout(int(timeout_ms), _stream_handle(stream))
 
 
 def attn_set_wait_timeout_ms(ms):

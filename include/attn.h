@@ -132,6 +132,16 @@ int attn_device_status(void* stream);
  */
 int attn_set_wait_timeout_ms(int ms);
 
+/*
+ * Failure-detection self-test (diagnostic; not part of the attention method).
+ * Enqueues on `stream` a one-thread kernel whose bounded device wait can never
+ * be satisfied, so the wait runs out after `timeout_ms` (1..10000) and sets the
+ * device error word: the next attn_device_status() returns
+ * ATTN_ERR_DEVICE_TIMEOUT (and clears it).  Nothing faults or hangs; the
+ * context stays usable.  Returns ATTN_ERR_INVALID_ARG for a limit out of range.
+ */
+int attn_selftest_wait_timeout(int timeout_ms, void* stream);
+
 /* Library ABI version: (major << 16) | minor. */
 int attn_version(void);
 

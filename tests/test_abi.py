@@ -103,3 +103,9 @@ def test_noalloc_backward_rejects_problems_beyond_its_fixed_scratch():
                               0.08, None, 0x6000, 0x7000, 0x8000, 0x9000)
     assert st == binding.ATTN_ERR_SCRATCH_LIMIT
     assert "scratch" in binding.status_text(st)
+
+
+def test_wait_timeout_selftest_rejects_out_of_range_limits():
+    lib = binding.load()
+    assert lib.attn_selftest_wait_timeout(0, None) == binding.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_wait_timeout(10001, None) == binding.ATTN_ERR_INVALID_ARG
