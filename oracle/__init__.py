@@ -38,22 +38,24 @@ def build(force=False):
     return _LIB_PATH
 
 
+def bind(lib):
+    """Sets the ctypes signatures of a loaded oracle library; returns it."""
+    d = ctypes.POINTER(ctypes.c_double)
+    i = ctypes.c_int
+    lib.oracle_fwd_rows.argtypes = [d, d, d, i, i, i, i, i, i, ctypes.c_double,
+                                    ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, d, d]
+    lib.oracle_fwd_rows.restype = i
+    lib.oracle_bwd.argtypes = [d, d, d, d, i, i, i, i, i, i, ctypes.c_double, d, d, d]
+    lib.oracle_bwd.restype = i
+    lib.oracle_num_threads.restype = i
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            d = ctypes.POINTER(ctypes.c_double)
-            i = ctypes.c_int
-            lib.oracle_fwd_rows.argtypes = [d, d, d, i, i, i, i, i, i, ctypes.c_double,
-                                            ctypes.POINTER(ctypes.c_int64), ctypes.c_int64,
-                                            d, d]
-            lib.oracle_fwd_rows.restype = i
-            lib.oracle_bwd.argtypes = [d, d, d, d, i, i, i, i, i, i, ctypes.c_double,
-                                       d, d, d]
-            lib.oracle_bwd.restype = i
-            lib.oracle_num_threads.restype = i
-            _lib = lib
+            _lib = bind(ctypes.CDLL(build()))
     return _lib
 
 
