@@ -12,6 +12,22 @@ size_t bwd_scratch_bytes(int B, int Hq, int N, int D) {
   return rows * (size_t)D * 4 + 2 * rows * 4;  // dQ accumulator, LSE2, Delta
 }
 
+size_t bwd_scratch_bytes_split(int B, int Hq, int Hkv, int N, int D, int gsplit) {
+  const size_t npad = ((size_t)N + 127) / 128 * 128;
+  const size_t kv = gsplit > 1 ? 2 * (size_t)B * Hkv * npad * (size_t)D * 4 : 0;
+  return bwd_scratch_bytes(B, Hq, N, D) + kv;
+}
+
+BwdScratch carve_scratch_split(void* base, int B, int Hq, int Hkv, int N, int D, int gsplit) {
+  BwdScratch s = carve_scratch(base, B, Hq, N, D);
+  if (gsplit > 1) {
+    const size_t npad = ((size_t)N + 127) / 128 * 128;
+    s.dk_acc = s.delta + (size_t)B * Hq * npad;
+    s.dv_acc = s.dk_acc + (size_t)B * Hkv * npad * D;
+  }
+  return s;
+}
+
 BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D) {
   const size_t npad = ((size_t)N + 127) / 128 * 128;
   const size_t rows = (size_t)B * Hq * npad;
@@ -19,6 +35,8 @@ BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D) {
   s.dq_acc = static_cast<float*>(base);
   s.lse2 = s.dq_acc + rows * D;
   s.delta = s.lse2 + rows;
+  s.dk_acc = nullptr;
+  s.dv_acc = nullptr;
   return s;
 }
 
@@ -27,7 +45,8 @@ BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D) {
 int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, int B, int Hq, int Hkv, int N, int D, float scale,
                        const void* dout, void* dq, void* dk, void* dv, BwdParams* p,
-                       CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo) {
+                       CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo,
+                       bool allow_split) {
   int st = validate_shape(B, Hq, Hkv, N, D, scale);
   if (st != ATTN_OK) return st;
   if ((long long)B * Hq * N == 0) return -1;  // nothing to do
@@ -56,6 +75,23 @@ int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
   p->scale_log2 = scale * 1.4426950408889634f;
   p->timeout_ns = wait_timeout_ns();
   p->err = err;
+  // One CTA per (key tile, batch, kv head) keeps a whole GQA group's dK/dV in
+  // TMEM.  When that grid is shorter than one wave, split the group's query
+  // heads over gsplit CTAs (the smallest divisor of G that fills the GPU).
+  p->gsplit = 1;
+  p->dk_acc = nullptr;
+  p->dv_acc = nullptr;
+  const long long ctas = (long long)p->num_kv_tiles * B * Hkv;
+  const int sms = device_sm_count(dev);
+  if (allow_split && p->G > 1 && ctas < sms) {
+    int g = p->G;
+    for (int d = 2; d <= p->G; ++d)
+      if (p->G % d == 0 && ctas * d >= sms) {
+        g = d;
+        break;
+      }
+    p->gsplit = g;
+  }
   return ATTN_OK;
 }
 
@@ -73,16 +109,19 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   BwdParams p;
   CUtensorMap tq, tk, tv, tdo;
   int st = bwd_prepare(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, dout, dq, dk, dv, &p, &tq, &tk,
-                       &tv, &tdo);
+                       &tv, &tdo, /*allow_split=*/true);
   if (st == -1) return ATTN_OK;
   if (st != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bwd_scratch_bytes(B, Hq, N, D), s) != cudaSuccess) return ATTN_ERR_CUDA;
-  const BwdScratch sc = carve_scratch(ws, B, Hq, N, D);
+  if (cudaMallocAsync(&ws, bwd_scratch_bytes_split(B, Hq, Hkv, N, D, p.gsplit), s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const BwdScratch sc = carve_scratch_split(ws, B, Hq, Hkv, N, D, p.gsplit);
   p.dq_acc = sc.dq_acc;
   p.lse2 = sc.lse2;
   p.delta = sc.delta;
+  p.dk_acc = sc.dk_acc;
+  p.dv_acc = sc.dv_acc;
   st = bwd_launch(tq, tk, tv, tdo, p, o, dout, lse, dq, D, causal, s);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == ATTN_OK) st = ATTN_ERR_CUDA;
   return st;

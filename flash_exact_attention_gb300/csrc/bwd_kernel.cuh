@@ -26,6 +26,11 @@
 //                   read it.
 //   bwd_postprocess dQ = scale * dQacc -> bf16.
 //
+// Group split (p.gsplit > 1, chosen by the host when one CTA per (key tile,
+// batch, kv head) would not fill the GPU): the query heads of a group are
+// divided over gsplit CTAs; each adds its fp32 dK/dV partials into fp32
+// accumulators by TMA reduce-add, and bwd_post_kv converts them to bf16.
+//
 // Warp roles of bwd_kernel (10 warps):
 //   0-7  compute warps.  Warp w covers TMEM lanes 32*(w%4).. and column half
 //        w/4: it computes dS for 64 of the 128 queries of its 32 key rows, then
@@ -60,8 +65,9 @@ struct BwdCfg {
   static constexpr int kdS = 6 * kTile;      // dS^T tile: 128 keys x 128 queries bf16
   static constexpr int kVec = kdS + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
   static constexpr int kBar = kVec + 2 * 1024;
-  // kv_full, qd_full[2], staged[2], s_ready, ds_ready, dq_ready, dq_free, all_done, red_go
-  static constexpr int kNumBars = 11;
+  // kv_full, qd_full[2], staged[2], s_ready, ds_ready, dq_ready, dq_free, all_done, red_go,
+  // prod_done, epi_staged[2]  (the last three only with a group split)
+  static constexpr int kNumBars = 14;
   static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
@@ -71,7 +77,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+               const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+               const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using Cfg = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -96,6 +103,10 @@ __global__ void __launch_bounds__(320, 1)
   // The producer has taken step it's staged dQ: the compute warps may signal
   // the next step's staging (keeps staged[] from running a phase ahead).
   const uint32_t bar_red_go = bar0 + 8u * 10;
+  // Group split only: the producer has finished with every ring stage, and the
+  // compute warps have staged their dV (half 0) / dK (half 1) partials.
+  const uint32_t bar_prod_done = bar0 + 8u * 11;
+  auto bar_epi = [&](int h) { return bar0 + 8u * (12 + h); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -111,6 +122,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_dq_free, 8);
     mbar_init(bar_done, 1);
     mbar_init(bar_red_go, 1);
+    mbar_init(bar_prod_done, 1);
+    mbar_init(bar_epi(0), 4);
+    mbar_init(bar_epi(1), 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -133,13 +147,19 @@ __global__ void __launch_bounds__(320, 1)
   // (smallest j) of all heads go first, for load balance.
   const int T = p.num_kv_tiles;
   const int BHkv = p.B * p.Hkv;
-  const int j = CAUSAL ? (int)blockIdx.x / BHkv : (int)blockIdx.x % T;
-  const int bhkv = CAUSAL ? (int)blockIdx.x % BHkv : (int)blockIdx.x / T;
+  const int GS = p.gsplit;  // CTAs per (key tile, batch, kv head)
+  const int j = CAUSAL ? (int)blockIdx.x / (BHkv * GS) : (int)blockIdx.x % T;
+  const int unit = CAUSAL ? (int)blockIdx.x % (BHkv * GS) : (int)blockIdx.x / T;
+  const int bhkv = unit / GS;
+  const int gi = unit % GS;  // which slice of the group's query heads
   const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
+  const int Gs = p.G / GS;  // query heads of this CTA
   const int i0 = CAUSAL ? j : 0;
   const int n_i = T - i0;
-  const int n_it = p.G * n_i;
-  auto q_head = [&](int it) { return b * p.Hq + hkv * p.G + it / n_i; };  // flat b*Hq + h
+  const int n_it = Gs * n_i;
+  auto q_head = [&](int it) {  // flat b*Hq + h
+    return b * p.Hq + hkv * p.G + gi * Gs + it / n_i;
+  };
   auto q_tile = [&](int it) { return i0 + it % n_i; };
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
   const uint32_t tS = tmem_base, tdP = tmem_base + 128, tdV = tmem_base + 256,
@@ -189,6 +209,19 @@ __global__ void __launch_bounds__(320, 1)
         if (ok && loaded < n_it) load_stage(loaded++);
       }
       bulk_wait_all();
+      if (ok && GS > 1) {
+        // Group split: every stage is free now; take the dV / dK partials the
+        // compute warps stage there and add them into the fp32 accumulators.
+        mbar_arrive(bar_prod_done);
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!(ok = mbar_wait(bar_epi(h), 0, wc))) break;
+          const uint32_t src = sbase + Cfg::kQ0 + h * 2 * Cfg::kTile;
+          for (int c = 0; c < D / 32; ++c)
+            tma_reduce_add_3d(h ? &tm_dk : &tm_dv, src + c * Cfg::kBox, c * 32, j * 128, bhkv);
+        }
+        bulk_commit();
+        bulk_wait_all();
+      }
       if (!ok) {
         // Let every load already issued land before the CTA can exit.
         for (int f = (loaded > 2 ? loaded - 2 : 0); f < loaded; ++f)
@@ -371,7 +404,31 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive(bar_staged(ch));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, wc));
-    if (ok) {
+    if (ok && GS > 1) {
+      // Group split: stage this row's fp32 dV (half 0) or unscaled dK (half 1)
+      // partial into ring stage `ch` for the producer's reduce-add.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_prod_done, 0, wc));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t src = (ch ? tdK : tdV) + lane_off;
+        const uint32_t stage = sbase + Cfg::kQ0 + ch * 2 * Cfg::kTile + (uint32_t)row * 128u;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld32(src + c * 32, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             stage + c * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
+                         "r"(rr[4 * v]), "r"(rr[4 * v + 1]), "r"(rr[4 * v + 2]), "r"(rr[4 * v + 3])
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_epi(ch));
+      }
+    } else if (ok) {
       // Epilogue: half 0 writes dV, half 1 writes dK (scaled) of this key row.
       tc_fence_after();
       const size_t orow = ((size_t)bhkv * p.N + (size_t)(key_live ? kj : 0)) * D;
@@ -414,7 +471,8 @@ __global__ void __launch_bounds__(256)
     bwd_preprocess(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                    const float* __restrict__ lse, float* __restrict__ lse2,
                    float* __restrict__ delta, float* __restrict__ dq_acc, long long rows, int N,
-                   int Npad) {
+                   int Npad, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
+                   long long kv_rows) {
   const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -448,6 +506,15 @@ __global__ void __launch_bounds__(256)
   float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)r * D);
 #pragma unroll
   for (int t = lane; t < D / 4; t += 32) z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (r < kv_rows) {  // group split: zero the dK/dV accumulators too
+    float4* zk = reinterpret_cast<float4*>(dk_acc + (size_t)r * D);
+    float4* zv = reinterpret_cast<float4*>(dv_acc + (size_t)r * D);
+#pragma unroll
+    for (int t = lane; t < D / 4; t += 32) {
+      zk[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
 }
 
 // dQ = scale * dQacc (rows < N) -> bf16.  8 elements per thread.
@@ -470,6 +537,35 @@ __global__ void __launch_bounds__(256)
   w.z = pack_bf16x2(c.x * scale, c.y * scale);
   w.w = pack_bf16x2(c.z * scale, c.w * scale);
   reinterpret_cast<uint4*>(dq + (size_t)r * D)[g] = w;
+}
+
+// Group split: dK = scale * dKacc, dV = dVacc (rows < N) -> bf16.  8 elements
+// per thread; rows are (b*Hkv + h)*N + i.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_post_kv(const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
+                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, long long rows,
+                int N, int Npad, float scale) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  constexpr int kGroups = D / 8;
+  const long long r = idx / kGroups;
+  if (r >= rows) return;
+  const int g = (int)(idx % kGroups);
+  const long long bh = r / N;
+  const int i = (int)(r % N);
+  const size_t off = ((size_t)bh * Npad + i) * D + g * 8;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const float4* src = reinterpret_cast<const float4*>((which ? dk_acc : dv_acc) + off);
+    const float m = which ? scale : 1.f;
+    const float4 a = src[0], c = src[1];
+    uint4 w;
+    w.x = pack_bf16x2(a.x * m, a.y * m);
+    w.y = pack_bf16x2(a.z * m, a.w * m);
+    w.z = pack_bf16x2(c.x * m, c.y * m);
+    w.w = pack_bf16x2(c.z * m, c.w * m);
+    reinterpret_cast<uint4*>((which ? dk : dv) + (size_t)r * D)[g] = w;
+  }
 }
 
 }  // namespace attn

@@ -11,23 +11,40 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
   using Cfg = BwdCfg<D>;
   CUtensorMap tdq;  // the fp32 dQ accumulator, target of the TMA reduce-add
   if (encode_f32_rows_map(&tdq, p.dq_acc, D, p.Npad, p.B * p.Hq) != 0) return cudaErrorInvalidValue;
+  // Group split: the fp32 dK/dV accumulators (else unused: any valid map).
+  CUtensorMap tdk = tdq, tdv = tdq;
+  const bool split = p.gsplit > 1;
+  if (split && (encode_f32_rows_map(&tdk, p.dk_acc, D, p.Npad, p.B * p.Hkv) != 0 ||
+                encode_f32_rows_map(&tdv, p.dv_acc, D, p.Npad, p.B * p.Hkv) != 0))
+    return cudaErrorInvalidValue;
   const long long prow = (long long)p.B * p.Hq * p.Npad;  // padded rows
+  const long long kv_rows = split ? (long long)p.B * p.Hkv * p.Npad : 0;
   bwd_preprocess<D><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse,
-      const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dq_acc, prow, p.N, p.Npad);
+      const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dq_acc, prow, p.N, p.Npad,
+      p.dk_acc, p.dv_acc, kv_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto kern = bwd_kernel<D, CAUSAL>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+  const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv) * (unsigned)p.gsplit;
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long orow = (long long)p.B * p.Hq * p.N;
   const long long groups = orow * (D / 8);
   bwd_postprocess<D><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
       p.dq_acc, static_cast<__nv_bfloat16*>(dq), orow, p.N, p.Npad, p.scale);
+  if (split) {
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long kvrow = (long long)p.B * p.Hkv * p.N;
+    const long long kvgroups = kvrow * (D / 8);
+    bwd_post_kv<D><<<(unsigned)((kvgroups + 255) / 256), 256, 0, stream>>>(
+        p.dk_acc, p.dv_acc, static_cast<__nv_bfloat16*>(p.dk), static_cast<__nv_bfloat16*>(p.dv),
+        kvrow, p.N, p.Npad, p.scale);
+  }
   return cudaGetLastError();
 }
 

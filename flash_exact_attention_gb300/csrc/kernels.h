@@ -36,6 +36,13 @@ struct BwdParams {
   float scale_log2;     // scale * log2(e)
   uint64_t timeout_ns;
   unsigned int* err;
+  // Query heads of a group are split over `gsplit` CTAs (1 = one CTA owns the
+  // whole group and writes dK/dV directly).  With gsplit > 1 each CTA adds its
+  // fp32 dK/dV partials into dk_acc / dv_acc ([B*Hkv, Npad, D], zeroed by the
+  // preprocess, converted by the postprocess).
+  int gsplit;
+  float* dk_acc;
+  float* dv_acc;
 };
 
 // Device pointers of the backward's fp32 scratch.
@@ -43,13 +50,21 @@ struct BwdScratch {
   float* dq_acc;
   float* lse2;
   float* delta;
+  float* dk_acc;  // only with gsplit > 1
+  float* dv_acc;
 };
 
 // Bytes of fp32 scratch the backward needs for these sizes.
 size_t bwd_scratch_bytes(int B, int Hq, int N, int D);
 
+// Bytes of fp32 scratch for a given group split (adds the dK/dV accumulators).
+size_t bwd_scratch_bytes_split(int B, int Hq, int Hkv, int N, int D, int gsplit);
+
 // Splits one scratch block of bwd_scratch_bytes() into its three arrays.
 BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D);
+
+// Same, with the dK/dV accumulators of a group split after them.
+BwdScratch carve_scratch_split(void* base, int B, int Hq, int Hkv, int N, int D, int gsplit);
 
 // Host-side validation and set-up of a backward call (tensor maps and every
 // parameter except the scratch pointers).  Returns ATTN_OK, an error code, or
@@ -57,7 +72,7 @@ BwdScratch carve_scratch(void* base, int B, int Hq, int N, int D);
 int bwd_prepare(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 int B, int Hq, int Hkv, int N, int D, float scale, const void* dout, void* dq,
                 void* dk, void* dv, BwdParams* p, CUtensorMap* tq, CUtensorMap* tk,
-                CUtensorMap* tv, CUtensorMap* tdo);
+                CUtensorMap* tv, CUtensorMap* tdo, bool allow_split = false);
 
 // Enqueues the three backward kernels with the scratch already in `p`.
 int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -108,3 +108,10 @@ def test_bwd_zero_query_gives_zero_dk():
     t["q"] = torch.zeros_like(t["q"])
     _, dk, _ = run_bwd(t, True, scale_for(64))
     assert float(dk.abs().max()) == 0.0
+
+
+def test_bwd_gqa_grid_of_more_than_one_wave_keeps_groups_whole():
+    """B=2, Hq=16, Hkv=8, N=2048, causal: 256 CTAs, so each CTA keeps its whole
+    query-head group (the smaller GQA cases above split groups over CTAs)."""
+    t = device_inputs(2, 16, 8, 2048, 128, 8, with_do=True)
+    check_bwd(t, True, scale_for(128))
