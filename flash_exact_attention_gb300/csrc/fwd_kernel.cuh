@@ -11,11 +11,17 @@
 // O += P V (tensor cores, fp32 in TMEM).  At the end O / l is written as bf16
 // and LSE = ln 2 * (m + log2 l).
 //
-// Warp roles (10 warps):
-//   warps 0-3  softmax for Q tile 0 (one thread per row, TMEM lanes 0-127)
-//   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into the ring
-//   warp  9    TMEM allocator and tcgen05.mma issuer
+// Warp roles (12 warps, three warpgroups):
+//   warps 0-3   softmax for Q tile 0 (one thread per row, TMEM lanes 0-127)
+//   warps 4-7   softmax for Q tile 1
+//   warp  8     TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into the ring
+//   warp  9     TMEM allocator and tcgen05.mma issuer
+//   warps 10-11 idle; they complete the third warpgroup for the register split
+// Registers: launched at 168 per thread (the cap when 3 warps share an SM
+// sub-partition); the third warpgroup gives registers back (setmaxnreg.dec to
+// 56) and the softmax warpgroups take them (224): 2*224 + 56 = 3*168.  With
+// 128 scores live per row, the extra registers let many exp2 chains be in
+// flight at once; at 168 the compiler could keep only a few.
 // MMA issue order per K/V tile j (two Q tiles ping-pong so that one tile's
 // softmax overlaps the other tile's matmuls):
 //   S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
@@ -56,12 +62,12 @@ struct FwdCfg {
   // barriers: q_full, full[kStages], empty[kStages], s_full[2], p_full[2], o_final
   static constexpr int kNumBars = 1 + 2 * kStages + 5;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + misc + alignment slack
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D>;
@@ -137,6 +143,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (lane == 0) {
       const int nq = has_t1 ? 2 : 1;
       mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
           const int s = (int)(it % ST);
           const uint32_t ph = (it / ST) & 1u;
-          ok = mbar_wait(bar_empty(s), ph ^ 1u, wc);
+          ok = mbar_wait_inl(bar_empty(s), ph ^ 1u, wc);
           if (!ok) break;
           mbar_arrive_expect_tx(bar_full(s), Cfg::kTileBytes);
           const CUtensorMap* tm = kv ? &tm_v : &tm_k;
@@ -162,12 +169,13 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
         for (uint32_t f = (it > (uint32_t)ST ? it - ST : 0); f < it; ++f)
-          mbar_wait_drain(bar_full((int)(f % ST)), (f / ST) & 1u, wc);
-        mbar_wait_drain(bar_q(), 0, wc);
+          mbar_wait_drain_inl(bar_full((int)(f % ST)), (f / ST) & 1u, wc);
+        mbar_wait_drain_inl(bar_q(), 0, wc);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0);
       constexpr uint32_t kIdescO = make_idesc_bf16(128, D, 1);
@@ -190,7 +198,7 @@ __global__ void __launch_bounds__(320, 1)
                  kIdescO, (acc || kk > 0) ? 1u : 0u);
       };
 
-      bool ok = mbar_wait(bar_q(), 0, wc);
+      bool ok = mbar_wait_inl(bar_q(), 0, wc);
       uint32_t it = 0, np0 = 0, np1 = 0;
       int sv_prev = 0;
       bool a1_prev = false;
@@ -202,14 +210,14 @@ __global__ void __launch_bounds__(320, 1)
         const int sv = (int)(it % ST);
         const uint32_t phv = (it / ST) & 1u;
         ++it;
-        if (!(ok = mbar_wait(bar_full(sk), phk, wc))) break;
+        if (!(ok = mbar_wait_inl(bar_full(sk), phk, wc))) break;
         tc_fence_after();
         if (a0) {
           issue_qk(0, ring(sk));
           mma_commit(bar_s(0));
         }
         if (j > 0 && a1_prev) {
-          if (!(ok = mbar_wait(bar_p(1), np1 & 1u, wc))) break;
+          if (!(ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) break;
           ++np1;
           tc_fence_after();
           issue_pv(1, ring(sv_prev), j - 1 > 0);
@@ -220,10 +228,10 @@ __global__ void __launch_bounds__(320, 1)
           mma_commit(bar_s(1));
         }
         mma_commit(bar_empty(sk));
-        if (!(ok = mbar_wait(bar_full(sv), phv, wc))) break;
+        if (!(ok = mbar_wait_inl(bar_full(sv), phv, wc))) break;
         tc_fence_after();
         if (a0) {
-          if (!(ok = mbar_wait(bar_p(0), np0 & 1u, wc))) break;
+          if (!(ok = mbar_wait_inl(bar_p(0), np0 & 1u, wc))) break;
           ++np0;
           tc_fence_after();
           issue_pv(0, ring(sv), j > 0);
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(320, 1)
         a1_prev = a1;
       }
       if (ok && a1_prev) {
-        if ((ok = mbar_wait(bar_p(1), np1 & 1u, wc))) {
+        if ((ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) {
           ++np1;
           tc_fence_after();
           issue_pv(1, ring(sv_prev), nkv - 1 > 0);
@@ -241,10 +249,13 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(bar_o());
       // On an aborted run nobody else may wait for the final commit: wait here
       // so that no MMA is in flight when TMEM is released.
-      if (!ok) mbar_wait_drain(bar_o(), 0, wc);
+      if (!ok) mbar_wait_drain_inl(bar_o(), 0, wc);
     }
+  } else if (warp >= 10) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
   } else {
     // ------------------------------------------------------------ softmax
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int j = 0; j < n_t; ++j) {
       // tcgen05.ld/st are warp-collective: keep the decision warp-uniform.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), (uint32_t)j & 1u, wc));
+      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_s(t), (uint32_t)j & 1u, wc));
       if (!ok) break;
       tc_fence_after();
       float s[128];
@@ -329,7 +340,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p(t));
     }
-    if (ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_o(), 0, wc));
+    if (ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), 0, wc));
     if (ok && n_t > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;

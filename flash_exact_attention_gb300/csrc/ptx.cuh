@@ -103,6 +103,37 @@ static __device__ __noinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parit
   }
 }
 
+// Fully inlined variants of mbar_wait / mbar_wait_drain for kernels that
+// change their register budget with setmaxnreg: ptxas cannot allocate
+// registers across a call to a non-inlined function inside such a region.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*wc.abort) return false;
+    if (global_timer_ns() - t0 > wc.timeout_ns) {
+      atomicOr(wc.err, kErrTimeout);
+      *wc.abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_drain_inl(uint32_t bar, uint32_t parity,
+                                                    const WaitCtl& wc) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > wc.timeout_ns) {
+      atomicOr(wc.err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 // 3-D tiled tensor load global -> shared, completing on an mbarrier (tx bytes).
 // c0 is the innermost coordinate in elements; c0 * sizeof(elem) must be a
