@@ -37,7 +37,10 @@
 //        stages half of the dQ columns of its 32 query rows, and at the end
 //        writes dV (half 0) or dK (half 1) of its key rows.
 //   8    TMA producer (K_j, V_j once; Q_i, dO_i, LSE2, Delta per iteration into a
-//        2-stage ring) and issuer of the dQ reduce-adds.
+//        2-stage ring) and issuer of the dQ reduce-adds.  Q and dO of a stage
+//        have separate barriers: the dQ half staged in the Q area is added
+//        first, so Q of step it+2 starts loading (D=128) while the dO-area
+//        half is still being read.
 //   9    TMEM allocator and MMA issuer.
 //
 // TMEM columns: [0,128) S^T, with P^T (bf16) of queries 0-63 written over
@@ -65,9 +68,9 @@ struct BwdCfg {
   static constexpr int kdS = 6 * kTile;      // dS^T tile: 128 keys x 128 queries bf16
   static constexpr int kVec = kdS + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
   static constexpr int kBar = kVec + 2 * 1024;
-  // kv_full, qd_full[2], staged[2], s_ready, ds_ready, dq_ready, dq_free, all_done, red_go,
-  // prod_done, epi_staged[2]  (the last three only with a group split)
-  static constexpr int kNumBars = 14;
+  // kv_full, qd_full[2] (dO, LSE2, Delta), staged[2], s_ready, ds_ready, dq_ready,
+  // dq_free, all_done, red_go, prod_done, epi_staged[2] (group split only), q_full[2]
+  static constexpr int kNumBars = 16;
   static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
@@ -93,7 +96,8 @@ __global__ void __launch_bounds__(320, 1)
 
   const uint32_t bar0 = sbase + Cfg::kBar;
   const uint32_t bar_kv = bar0;
-  auto bar_qd_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_qd_full = [&](int s) { return bar0 + 8u * (1 + s); };   // dO_i, LSE2, Delta landed
+  auto bar_q_full = [&](int s) { return bar0 + 8u * (14 + s); };   // Q_i landed
   auto bar_staged = [&](int h) { return bar0 + 8u * (3 + h); };  // dQ column half h staged
   const uint32_t bar_s = bar0 + 8u * 5;
   const uint32_t bar_ds = bar0 + 8u * 6;
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_qd_full(s), 1);
+      mbar_init(bar_q_full(s), 1);
       mbar_init(bar_staged(s), 4);
     }
     mbar_init(bar_s, 1);
@@ -173,19 +178,28 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sbase + Cfg::kK + c * Cfg::kBox, &tm_k, bar_kv, c * 64, j * 128, bhkv);
         tma_load_3d(sbase + Cfg::kV + c * Cfg::kBox, &tm_v, bar_kv, c * 64, j * 128, bhkv);
       }
-      auto load_stage = [&](int it) {
+      auto load_q = [&](int it) {
+        const int s = it & 1;
+        const uint32_t qs = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
+        mbar_arrive_expect_tx(bar_q_full(s), Cfg::kTile);
+        for (int c = 0; c < Cfg::kBoxes; ++c)
+          tma_load_3d(qs + c * Cfg::kBox, &tm_q, bar_q_full(s), c * 64, q_tile(it) * 128, q_head(it));
+      };
+      auto load_do = [&](int it) {
         const int s = it & 1;
         const int bhq = q_head(it), i = q_tile(it);
         const uint32_t qs = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
-        mbar_arrive_expect_tx(bar_qd_full(s), 2 * Cfg::kTile + 1024);
-        for (int c = 0; c < Cfg::kBoxes; ++c) {
-          tma_load_3d(qs + c * Cfg::kBox, &tm_q, bar_qd_full(s), c * 64, i * 128, bhq);
+        mbar_arrive_expect_tx(bar_qd_full(s), Cfg::kTile + 1024);
+        for (int c = 0; c < Cfg::kBoxes; ++c)
           tma_load_3d(qs + Cfg::kTile + c * Cfg::kBox, &tm_do, bar_qd_full(s), c * 64, i * 128,
                       bhq);
-        }
         const size_t voff = (size_t)bhq * p.Npad + (size_t)i * 128;
         bulk_load(sbase + Cfg::kVec + s * 1024, p.lse2 + voff, 512, bar_qd_full(s));
         bulk_load(sbase + Cfg::kVec + s * 1024 + 512, p.delta + voff, 512, bar_qd_full(s));
+      };
+      auto load_stage = [&](int it) {
+        load_q(it);
+        load_do(it);
       };
       int loaded = 0;
       for (; loaded < 2 && loaded < n_it; ++loaded) load_stage(loaded);
@@ -193,6 +207,8 @@ __global__ void __launch_bounds__(320, 1)
       for (int it = 0; it < n_it && ok; ++it) {
         // dQ_it was staged in stage it&1 (its MMAs are all complete by then):
         // add it to the accumulator half by half, then reuse the stage.
+        // Half 0 of dQ_it was staged in the Q area of the stage, half 1 in the
+        // dO area: as soon as half 0 has been read, Q for step it+2 can load.
         const uint32_t stage = sbase + Cfg::kQ0 + (it & 1) * 2 * Cfg::kTile;
         for (int h = 0; h < 2 && ok; ++h) {
           if (!(ok = mbar_wait(bar_staged(h), (uint32_t)it & 1u, wc))) break;
@@ -202,11 +218,18 @@ __global__ void __launch_bounds__(320, 1)
             tma_reduce_add_3d(&tm_dq, stage + c * Cfg::kBox, c * 32, q_tile(it) * 128,
                               q_head(it));
           }
+          bulk_commit();
         }
-        bulk_commit();
         if (ok) mbar_arrive(bar_red_go);
-        bulk_wait_read_all();
-        if (ok && loaded < n_it) load_stage(loaded++);
+        if constexpr (D == 128) {
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          if (ok && loaded < n_it) load_q(loaded);
+          bulk_wait_read_all();
+          if (ok && loaded < n_it) load_do(loaded++);
+        } else {  // at D=64 reloading the whole stage at once measured faster
+          bulk_wait_read_all();
+          if (ok && loaded < n_it) load_stage(loaded++);
+        }
       }
       bulk_wait_all();
       if (ok && GS > 1) {
@@ -224,8 +247,10 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (!ok) {
         // Let every load already issued land before the CTA can exit.
-        for (int f = (loaded > 2 ? loaded - 2 : 0); f < loaded; ++f)
+        for (int f = (loaded > 2 ? loaded - 2 : 0); f < loaded; ++f) {
+          mbar_wait_drain(bar_q_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
           mbar_wait_drain(bar_qd_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
+        }
         mbar_wait_drain(bar_kv, 0, wc);
       }
     }
@@ -266,7 +291,8 @@ __global__ void __launch_bounds__(320, 1)
                  make_sdesc_sw128(k_addr + kk * 2048, Cfg::kBox, 1024), kIdescDQ, kk > 0);
       };
 
-      bool ok = mbar_wait(bar_kv, 0, wc) && mbar_wait(bar_qd_full(0), 0, wc);
+      bool ok = mbar_wait(bar_kv, 0, wc) && mbar_wait(bar_q_full(0), 0, wc) &&
+                mbar_wait(bar_qd_full(0), 0, wc);
       if (ok) {
         tc_fence_after();
         issue_t(tS, k_addr, q_addr(0));
@@ -281,10 +307,11 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(bar_dq);  // the dQ warps release stage s after staging dQ in it
         if (it + 1 < n_it) {
           const int s1 = (it + 1) & 1;
-          if (!(ok = mbar_wait(bar_qd_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
+          if (!(ok = mbar_wait(bar_q_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
           tc_fence_after();
           issue_t(tS, k_addr, q_addr(s1));
           if (!(ok = mbar_wait(bar_dq_free, (uint32_t)it & 1u, wc))) break;
+          if (!(ok = mbar_wait(bar_qd_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
           tc_fence_after();
           issue_t(tdP, v_addr, do_addr(s1));
           mma_commit(bar_s);
