@@ -16,14 +16,16 @@
 //                     dP^T = V_j dO_i^T           (tcgen05, TMEM)
 //                     P^T  = 2^(S^T c - LSE2_i), dS^T = P^T o (dP^T - Delta_i)
 //                     dV_j += P^T dO_i            (A = P^T from TMEM)
+//                     dQ_i  = dS K_j              (A = the dS^T tile read MN-major)
 //                     dK_j += dS^T Q_i            (A = dS^T from shared memory)
-//                     dQ_i  = dS K_j              (A = the same dS^T tile read MN-major)
 //                   dK/dV stay in TMEM across the whole group (no GQA reduction
-//                   pass).  dQ_i goes TMEM -> registers -> the Q_i/dO_i ring
-//                   stage (dead once the dQ MMA has finished) -> TMA tensor
-//                   reduce-add into the fp32 accumulator, issued by the producer
-//                   thread, which reloads the stage as soon as the reduce-add has
-//                   read it.
+//                   pass).  The tensor cores run, per query tile i,
+//                     dP_i, dV_i, S_{i+1}, dQ_i, dK_i
+//                   so that P_{i+1} is computed while dQ_i, dK_i and dP_{i+1}
+//                   run, and dS_i while dV_i and S_{i+1} run.  dQ_i goes TMEM ->
+//                   registers of a dedicated warpgroup (freeing the columns for
+//                   dP_{i+1} at once) -> a two-slot shared staging ring -> TMA
+//                   tensor reduce-add into the fp32 accumulator.
 //   bwd_postprocess dQ = scale * dQacc -> bf16.
 //
 // Group split (p.gsplit > 1, chosen by the host when one CTA per (key tile,
@@ -31,17 +33,20 @@
 // divided over gsplit CTAs; each adds its fp32 dK/dV partials into fp32
 // accumulators by TMA reduce-add, and bwd_post_kv converts them to bf16.
 //
-// Warp roles of bwd_kernel (10 warps):
-//   0-7  compute warps.  Warp w covers TMEM lanes 32*(w%4).. and column half
-//        w/4: it computes dS for 64 of the 128 queries of its 32 key rows, then
-//        stages half of the dQ columns of its 32 query rows, and at the end
-//        writes dV (half 0) or dK (half 1) of its key rows.
-//   8    TMA producer (K_j, V_j once; Q_i, dO_i, LSE2, Delta per iteration into a
-//        2-stage ring) and issuer of the dQ reduce-adds.  Q and dO of a stage
-//        have separate barriers: the dQ half staged in the Q area is added
-//        first, so Q of step it+2 starts loading (D=128) while the dO-area
-//        half is still being read.
-//   9    TMEM allocator and MMA issuer.
+// Warp roles of bwd_kernel (16 warps):
+//   0-7   compute warps.  Warp w covers TMEM lanes 32*(w%4).. (32 keys) and
+//         query half w/4: P for 64 queries of its key rows (kept in registers,
+//         written to TMEM as bf16 for the dV MMA), then dS for the same
+//         queries; at the end it writes dV (half 0) or dK (half 1).
+//   8-11  dQ warpgroup (thread = query row): dQ_i out of TMEM, staged 32
+//         columns (16 KB) at a time, reduce-adds issued by its first thread.
+//   12    TMA producer: K_j, V_j once; Q_i with LSE2_i and Delta_i into a
+//         2-stage ring; dO_i into a single buffer (reloaded once dV_i is done).
+//   13    TMEM allocator and MMA issuer.
+//   14-15 idle (they complete the fourth warpgroup for the register split).
+// Registers: launched at 128 per thread; setmaxnreg moves them to the compute
+// warps (144: P of 64 queries stays live across the dS step) and the dQ
+// warpgroup (168: a whole fp32 dQ row), 8*144 + 4*168 + 4*56 = 16*128.
 //
 // TMEM columns: [0,128) S^T, with P^T (bf16) of queries 0-63 written over
 // columns [0,32) and of queries 64-127 over [64,96) (each half stays inside the
@@ -57,27 +62,40 @@ namespace attn {
 
 constexpr unsigned kErrSmemAlign = 2u;  // device error bit: shared memory base misaligned
 
+template <int V>
+struct IntConst {
+  static constexpr int value = V;
+};
+
 template <int D>
 struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;  // one 128-row bf16 tile
-  static constexpr int kBox = 128 * 128;     // one 64-column box (128-byte rows)
-  static constexpr int kBoxes = D / 64;
+  static constexpr int kBox = 128 * 128;     // one 128-row box of 128-byte rows
+  static constexpr int kBoxes = D / 64;      // bf16 boxes per tile
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
-  static constexpr int kQ0 = 2 * kTile;      // stage s: Q at kQ0 + s*2*kTile, dO right after
-  static constexpr int kdS = 6 * kTile;      // dS^T tile: 128 keys x 128 queries bf16
-  static constexpr int kVec = kdS + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
+  static constexpr int kQ0 = 2 * kTile;        // Q stage s at kQ0 + s * kTile
+  static constexpr int kdO = 4 * kTile;
+  static constexpr int kdS = 5 * kTile;        // dS^T tile: 128 keys x 128 queries bf16
+  static constexpr int kdQ = kdS + 2 * kBox;   // dQ staging: 2 slots of 128 rows x 32 fp32
+  static constexpr int kVec = kdQ + 2 * kBox;  // stage s: LSE2[128] then Delta[128]
   static constexpr int kBar = kVec + 2 * 1024;
-  // kv_full, qd_full[2] (dO, LSE2, Delta), staged[2], s_ready, ds_ready, dq_ready,
-  // dq_free, all_done, red_go, prod_done, epi_staged[2] (group split only), q_full[2]
   static constexpr int kNumBars = 16;
   static constexpr int kSmemBytes = kBar + kNumBars * 8 + 16;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 512;
   static constexpr uint32_t kTmemCols = 512;
+  // Register split (per thread): 8 compute warps, 4 dQ warps, 4 other warps.
+  static constexpr int kRegCompute = 144, kRegDq = 168, kRegOther = 56;
+  static_assert(8 * kRegCompute + 4 * kRegDq + 4 * kRegOther == 16 * launch_regs(kThreads),
+                "the register split must add up to the launch allocation");
+  // Group split: the fp32 dV / dK partials (D/32 boxes each) are staged over
+  // the Q ring and over dO + dS, all free once the last MMA has completed.
+  static_assert(2 * kTile >= (D / 32) * kBox, "dV partial staging");
+  static_assert(kTile + 2 * kBox >= (D / 32) * kBox, "dK partial staging");
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
@@ -96,45 +114,42 @@ __global__ void __launch_bounds__(320, 1)
 
   const uint32_t bar0 = sbase + Cfg::kBar;
   const uint32_t bar_kv = bar0;
-  auto bar_qd_full = [&](int s) { return bar0 + 8u * (1 + s); };   // dO_i, LSE2, Delta landed
-  auto bar_q_full = [&](int s) { return bar0 + 8u * (14 + s); };   // Q_i landed
-  auto bar_staged = [&](int h) { return bar0 + 8u * (3 + h); };  // dQ column half h staged
-  const uint32_t bar_s = bar0 + 8u * 5;
-  const uint32_t bar_ds = bar0 + 8u * 6;
-  const uint32_t bar_dq = bar0 + 8u * 7;
-  const uint32_t bar_dq_free = bar0 + 8u * 8;
-  const uint32_t bar_done = bar0 + 8u * 9;
-  // The producer has taken step it's staged dQ: the compute warps may signal
-  // the next step's staging (keeps staged[] from running a phase ahead).
-  const uint32_t bar_red_go = bar0 + 8u * 10;
-  // Group split only: the producer has finished with every ring stage, and the
-  // compute warps have staged their dV (half 0) / dK (half 1) partials.
-  const uint32_t bar_prod_done = bar0 + 8u * 11;
-  auto bar_epi = [&](int h) { return bar0 + 8u * (12 + h); };
+  auto bar_q_full = [&](int s) { return bar0 + 8u * (1 + s); };  // Q, LSE2, Delta of stage s
+  auto bar_q_free = [&](int s) { return bar0 + 8u * (3 + s); };  // dK MMA done with stage s
+  const uint32_t bar_do_full = bar0 + 8u * 5;
+  const uint32_t bar_do_free = bar0 + 8u * 6;   // dV MMA done with dO
+  const uint32_t bar_s = bar0 + 8u * 7;         // S^T complete
+  const uint32_t bar_p = bar0 + 8u * 8;         // P^T in TMEM (8 compute warps)
+  const uint32_t bar_dp = bar0 + 8u * 9;        // dP^T complete
+  const uint32_t bar_ds = bar0 + 8u * 10;       // dS^T in shared memory (8 compute warps)
+  const uint32_t bar_dq = bar0 + 8u * 11;       // dQ complete in TMEM
+  const uint32_t bar_dq_free = bar0 + 8u * 12;  // dQ read out of TMEM (4 dQ warps)
+  const uint32_t bar_done = bar0 + 8u * 13;     // every MMA complete
+  auto bar_epi = [&](int h) { return bar0 + 8u * (14 + h); };  // group split: partial staged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBar + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_qd_full(s), 1);
       mbar_init(bar_q_full(s), 1);
-      mbar_init(bar_staged(s), 4);
+      mbar_init(bar_q_free(s), 1);
+      mbar_init(bar_epi(s), 4);
     }
+    mbar_init(bar_do_full, 1);
+    mbar_init(bar_do_free, 1);
     mbar_init(bar_s, 1);
+    mbar_init(bar_p, 8);
+    mbar_init(bar_dp, 1);
     mbar_init(bar_ds, 8);
     mbar_init(bar_dq, 1);
-    mbar_init(bar_dq_free, 8);
+    mbar_init(bar_dq_free, 4);
     mbar_init(bar_done, 1);
-    mbar_init(bar_red_go, 1);
-    mbar_init(bar_prod_done, 1);
-    mbar_init(bar_epi(0), 4);
-    mbar_init(bar_epi(1), 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
-  if (warp == 8 && lane == 0) {
+  if (warp == 13) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -148,8 +163,9 @@ __global__ void __launch_bounds__(320, 1)
 
   // ---- work unit: (key tile j, batch, kv head).  Non-causal: the key tiles of
   // one head are consecutive, so the CTAs resident at one time share a few
-  // heads' Q, dO and dQ accumulator in L2.  Causal: the heaviest key tiles
-  // (smallest j) of all heads go first, for load balance.
+  // heads' Q, dO and dQ accumulator in L2, and each starts its query loop at
+  // tile j so that they add into different dQ tiles at any one time.  Causal:
+  // the heaviest key tiles (smallest j) of all heads go first, for load balance.
   const int T = p.num_kv_tiles;
   const int BHkv = p.B * p.Hkv;
   const int GS = p.gsplit;  // CTAs per (key tile, batch, kv head)
@@ -165,166 +181,212 @@ __global__ void __launch_bounds__(320, 1)
   auto q_head = [&](int it) {  // flat b*Hq + h
     return b * p.Hq + hkv * p.G + gi * Gs + it / n_i;
   };
-  auto q_tile = [&](int it) { return i0 + it % n_i; };
+  auto q_tile = [&](int it) {
+    const int r = it % n_i;
+    return CAUSAL ? i0 + r : (r + j) % T;
+  };
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
   const uint32_t tS = tmem_base, tdP = tmem_base + 128, tdV = tmem_base + 256,
                  tdK = tmem_base + 256 + D;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer + dQ reduce
-    if (lane == 0) {
+  if (warp >= 12) {
+    regs_decrease<Cfg::kRegOther>();
+    if (warp == 12 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       mbar_arrive_expect_tx(bar_kv, 2 * Cfg::kTile);
       for (int c = 0; c < Cfg::kBoxes; ++c) {
         tma_load_3d(sbase + Cfg::kK + c * Cfg::kBox, &tm_k, bar_kv, c * 64, j * 128, bhkv);
         tma_load_3d(sbase + Cfg::kV + c * Cfg::kBox, &tm_v, bar_kv, c * 64, j * 128, bhkv);
       }
-      auto load_q = [&](int it) {
-        const int s = it & 1;
-        const uint32_t qs = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
-        mbar_arrive_expect_tx(bar_q_full(s), Cfg::kTile);
-        for (int c = 0; c < Cfg::kBoxes; ++c)
-          tma_load_3d(qs + c * Cfg::kBox, &tm_q, bar_q_full(s), c * 64, q_tile(it) * 128, q_head(it));
-      };
-      auto load_do = [&](int it) {
+      auto load_q = [&](int it) {  // Q_i, LSE2_i, Delta_i into stage it&1
         const int s = it & 1;
         const int bhq = q_head(it), i = q_tile(it);
-        const uint32_t qs = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile;
-        mbar_arrive_expect_tx(bar_qd_full(s), Cfg::kTile + 1024);
+        const uint32_t qs = sbase + Cfg::kQ0 + s * Cfg::kTile;
+        mbar_arrive_expect_tx(bar_q_full(s), Cfg::kTile + 1024);
         for (int c = 0; c < Cfg::kBoxes; ++c)
-          tma_load_3d(qs + Cfg::kTile + c * Cfg::kBox, &tm_do, bar_qd_full(s), c * 64, i * 128,
-                      bhq);
+          tma_load_3d(qs + c * Cfg::kBox, &tm_q, bar_q_full(s), c * 64, i * 128, bhq);
         const size_t voff = (size_t)bhq * p.Npad + (size_t)i * 128;
-        bulk_load(sbase + Cfg::kVec + s * 1024, p.lse2 + voff, 512, bar_qd_full(s));
-        bulk_load(sbase + Cfg::kVec + s * 1024 + 512, p.delta + voff, 512, bar_qd_full(s));
+        bulk_load(sbase + Cfg::kVec + s * 1024, p.lse2 + voff, 512, bar_q_full(s));
+        bulk_load(sbase + Cfg::kVec + s * 1024 + 512, p.delta + voff, 512, bar_q_full(s));
       };
-      auto load_stage = [&](int it) {
-        load_q(it);
-        load_do(it);
+      auto load_do = [&](int it) {
+        mbar_arrive_expect_tx(bar_do_full, Cfg::kTile);
+        for (int c = 0; c < Cfg::kBoxes; ++c)
+          tma_load_3d(sbase + Cfg::kdO + c * Cfg::kBox, &tm_do, bar_do_full, c * 64,
+                      q_tile(it) * 128, q_head(it));
       };
-      int loaded = 0;
-      for (; loaded < 2 && loaded < n_it; ++loaded) load_stage(loaded);
+      load_q(0);
+      load_do(0);
+      if (n_it > 1) load_q(1);
+      int nq = n_it > 1 ? 2 : 1, ndo = 1;  // loads issued
       bool ok = true;
       for (int it = 0; it < n_it && ok; ++it) {
-        // dQ_it was staged in stage it&1 (its MMAs are all complete by then):
-        // add it to the accumulator half by half, then reuse the stage.
-        // Half 0 of dQ_it was staged in the Q area of the stage, half 1 in the
-        // dO area: as soon as half 0 has been read, Q for step it+2 can load.
-        const uint32_t stage = sbase + Cfg::kQ0 + (it & 1) * 2 * Cfg::kTile;
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait(bar_staged(h), (uint32_t)it & 1u, wc))) break;
-#pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {
-            const int c = h * (D / 64) + cc;  // 32-column box
-            tma_reduce_add_3d(&tm_dq, stage + c * Cfg::kBox, c * 32, q_tile(it) * 128,
-                              q_head(it));
-          }
-          bulk_commit();
+        if (it + 1 < n_it) {
+          if (!(ok = mbar_wait_inl(bar_do_free, (uint32_t)it & 1u, wc))) break;
+          load_do(it + 1);
+          ++ndo;
         }
-        if (ok) mbar_arrive(bar_red_go);
-        if constexpr (D == 128) {
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          if (ok && loaded < n_it) load_q(loaded);
-          bulk_wait_read_all();
-          if (ok && loaded < n_it) load_do(loaded++);
-        } else {  // at D=64 reloading the whole stage at once measured faster
-          bulk_wait_read_all();
-          if (ok && loaded < n_it) load_stage(loaded++);
+        if (it + 2 < n_it) {
+          if (!(ok = mbar_wait_inl(bar_q_free(it & 1), (uint32_t)(it >> 1) & 1u, wc))) break;
+          load_q(it + 2);
+          ++nq;
         }
-      }
-      bulk_wait_all();
-      if (ok && GS > 1) {
-        // Group split: every stage is free now; take the dV / dK partials the
-        // compute warps stage there and add them into the fp32 accumulators.
-        mbar_arrive(bar_prod_done);
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!(ok = mbar_wait(bar_epi(h), 0, wc))) break;
-          const uint32_t src = sbase + Cfg::kQ0 + h * 2 * Cfg::kTile;
-          for (int c = 0; c < D / 32; ++c)
-            tma_reduce_add_3d(h ? &tm_dk : &tm_dv, src + c * Cfg::kBox, c * 32, j * 128, bhkv);
-        }
-        bulk_commit();
-        bulk_wait_all();
       }
       if (!ok) {
         // Let every load already issued land before the CTA can exit.
-        for (int f = (loaded > 2 ? loaded - 2 : 0); f < loaded; ++f) {
-          mbar_wait_drain(bar_q_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
-          mbar_wait_drain(bar_qd_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
-        }
-        mbar_wait_drain(bar_kv, 0, wc);
+        for (int f = (nq > 2 ? nq - 2 : 0); f < nq; ++f)
+          mbar_wait_drain_inl(bar_q_full(f & 1), (uint32_t)(f >> 1) & 1u, wc);
+        mbar_wait_drain_inl(bar_do_full, (uint32_t)(ndo - 1) & 1u, wc);
+        mbar_wait_drain_inl(bar_kv, 0, wc);
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 13 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t kIdescB_MN = make_idesc_bf16(128, D, 1, 0);  // dV, dK
       constexpr uint32_t kIdescDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A and B MN-major
-      const uint32_t k_addr = sbase + Cfg::kK, v_addr = sbase + Cfg::kV, ds_addr = sbase + Cfg::kdS;
-      auto q_addr = [&](int s) { return sbase + Cfg::kQ0 + s * 2 * Cfg::kTile; };
-      auto do_addr = [&](int s) { return sbase + Cfg::kQ0 + s * 2 * Cfg::kTile + Cfg::kTile; };
+      constexpr uint32_t kHi = sdesc_sw128_hi(1024);  // 8-row groups 1024 bytes apart
+      // Address words of every operand, K-major (K advances inside a 128-byte
+      // row, then by a 64-column box) or MN-major (K advances by 16 rows; the
+      // 64-element MN chunks are one box apart).
+      const uint32_t kK = sdesc_sw128_lo(sbase + Cfg::kK, 16);
+      const uint32_t kV = sdesc_sw128_lo(sbase + Cfg::kV, 16);
+      const uint32_t kdO = sdesc_sw128_lo(sbase + Cfg::kdO, 16);
+      const uint32_t kdS = sdesc_sw128_lo(sbase + Cfg::kdS, 16);
+      const uint32_t mdO = sdesc_sw128_lo(sbase + Cfg::kdO, Cfg::kBox);
+      const uint32_t mdS = sdesc_sw128_lo(sbase + Cfg::kdS, Cfg::kBox);
+      const uint32_t mK = sdesc_sw128_lo(sbase + Cfg::kK, Cfg::kBox);
+      const uint32_t kQ0 = sdesc_sw128_lo(sbase + Cfg::kQ0, 16);
+      const uint32_t mQ0 = sdesc_sw128_lo(sbase + Cfg::kQ0, Cfg::kBox);
+      constexpr uint32_t kQs = Cfg::kTile >> 4;  // stage stride in address units
+      // K-step kk of a K-major operand: (kk/4) boxes + (kk%4) 32-byte steps;
+      // of an MN-major operand: kk * 16 rows of 128 bytes.
+      auto koff = [](int kk) { return (uint32_t)(((kk / 4) * Cfg::kBox + (kk % 4) * 32) >> 4); };
+      auto moff = [](int kk) { return (uint32_t)((kk * 2048) >> 4); };
       // X^T = A B^T with A a [128 x D] K-major tile (K or V), B a [128 x D] K-major tile.
       auto issue_t = [&](uint32_t dst, uint32_t a, uint32_t bb) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * Cfg::kBox + (kk % 4) * 32;
-          mma_ss(dst, make_sdesc_sw128(a + off, 16, 1024), make_sdesc_sw128(bb + off, 16, 1024),
-                 kIdescSS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_w(dst, a, koff(kk), bb, koff(kk), kHi, kIdescSS, kk > 0);
       };
-      auto issue_grads = [&](int s, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO  (K = 128 queries)
-          mma_ts(tdV, tS + (kk / 4) * 64 + (kk % 4) * 8,
-                 make_sdesc_sw128(do_addr(s) + kk * 2048, Cfg::kBox, 1024), kIdescB_MN,
-                 (acc || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q  (K = 128 queries)
-          const uint32_t off = (kk / 4) * Cfg::kBox + (kk % 4) * 32;
-          mma_ss(tdK, make_sdesc_sw128(ds_addr + off, 16, 1024),
-                 make_sdesc_sw128(q_addr(s) + kk * 2048, Cfg::kBox, 1024), kIdescB_MN,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys), into the dP^T columns
-          mma_ss(tdP, make_sdesc_sw128(ds_addr + kk * 2048, Cfg::kBox, 1024),
-                 make_sdesc_sw128(k_addr + kk * 2048, Cfg::kBox, 1024), kIdescDQ, kk > 0);
-      };
-
-      bool ok = mbar_wait(bar_kv, 0, wc) && mbar_wait(bar_q_full(0), 0, wc) &&
-                mbar_wait(bar_qd_full(0), 0, wc);
-      if (ok) {
+      // One query tile: dP_it, dV_it, S_{it+1}, dK_it, dQ_it.  The stage s = it & 1
+      // is a compile-time constant, so every descriptor is a register plus an
+      // immediate.
+      auto step = [&](int it, auto stage) -> bool {
+        constexpr int s = decltype(stage)::value;
+        const uint32_t mQs_ = mQ0 + s * kQs, kQn = kQ0 + (s ^ 1) * kQs;
+        // dP_it over the dP^T columns, once dQ_{it-1} has been read out of them.
+        if (it > 0 && !mbar_wait_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc)) return false;
+        if (!mbar_wait_inl(bar_do_full, (uint32_t)it & 1u, wc)) return false;
         tc_fence_after();
-        issue_t(tS, k_addr, q_addr(0));
-        issue_t(tdP, v_addr, do_addr(0));
-        mma_commit(bar_s);
-      }
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it & 1;
-        if (!(ok = mbar_wait(bar_ds, (uint32_t)it & 1u, wc))) break;
+        issue_t(tdP, kV, kdO);
+        mma_commit(bar_dp);
+        // dV += P^T dO  (K = 128 queries; A = P^T from TMEM)
+        if (!mbar_wait_inl(bar_p, (uint32_t)it & 1u, wc)) return false;
         tc_fence_after();
-        issue_grads(s, it > 0);
-        mma_commit(bar_dq);  // the dQ warps release stage s after staging dQ in it
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_w(tdV, tS + (kk / 4) * 64 + (kk % 4) * 8, mdO, moff(kk), kHi, kIdescB_MN,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar_do_free);
+        // S_{it+1} over the S^T columns (P^T_it has been consumed by dV, in order).
         if (it + 1 < n_it) {
-          const int s1 = (it + 1) & 1;
-          if (!(ok = mbar_wait(bar_q_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
+          if (!mbar_wait_inl(bar_q_full(s ^ 1), (uint32_t)((it + 1) >> 1) & 1u, wc)) return false;
           tc_fence_after();
-          issue_t(tS, k_addr, q_addr(s1));
-          if (!(ok = mbar_wait(bar_dq_free, (uint32_t)it & 1u, wc))) break;
-          if (!(ok = mbar_wait(bar_qd_full(s1), (uint32_t)((it + 1) >> 1) & 1u, wc))) break;
-          tc_fence_after();
-          issue_t(tdP, v_addr, do_addr(s1));
+          issue_t(tS, kK, kQn);
           mma_commit(bar_s);
         }
+        if (!mbar_wait_inl(bar_ds, (uint32_t)it & 1u, wc)) return false;
+        tc_fence_after();
+        // dK += dS^T Q first: it frees Q stage s for the producer one MMA group earlier.
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_w(tdK, kdS, koff(kk), mQs_, moff(kk), kHi, kIdescB_MN,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar_q_free(s));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys), into the dP^T columns
+          mma_ss_w(tdP, mdS, moff(kk), mK, moff(kk), kHi, kIdescDQ, kk > 0);
+        mma_commit(bar_dq);
+        return true;
+      };
+      bool ok = mbar_wait_inl(bar_kv, 0, wc) && mbar_wait_inl(bar_q_full(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        issue_t(tS, kK, kQ0);
+        mma_commit(bar_s);
+      }
+      for (int it = 0; it < n_it && ok; it += 2) {
+        ok = step(it, IntConst<0>{});
+        if (ok && it + 1 < n_it) ok = step(it + 1, IntConst<1>{});
       }
       mma_commit(bar_done);
-      if (!ok) mbar_wait_drain(bar_done, 0, wc);
+      if (!ok) mbar_wait_drain_inl(bar_done, 0, wc);
     }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ warpgroup
+    regs_increase<Cfg::kRegDq>();
+    const int wq = warp & 3;
+    const int qrow = wq * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const bool leader = warp == 8 && lane == 0;
+    const uint32_t swz = (uint32_t)(qrow & 7);
+    const uint32_t st_row = sbase + Cfg::kdQ + (uint32_t)qrow * 128u;
+    int chunk = 0;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      // One decision for the whole warpgroup: its named barriers need all 4 warps.
+      ok = named_bar_and(1, 128, mbar_wait_inl(bar_dq, (uint32_t)it & 1u, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[D / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tdP + lane_off + cc * 32, r[cc]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_free);
+      const int qt = q_tile(it), qh = q_head(it);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc, ++chunk) {
+        const uint32_t slot = (uint32_t)(chunk & 1) * Cfg::kBox;
+        // The slot's previous reduce-add (two chunks ago) must have read it.
+        if (leader) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        named_bar_sync(1, 128);
+        // 128-byte rows, 16-byte chunks swizzled by row & 7 (the map's 128B swizzle).
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           st_row + slot + ((((uint32_t)v) ^ swz) << 4)),
+                       "r"(r[cc][4 * v]), "r"(r[cc][4 * v + 1]), "r"(r[cc][4 * v + 2]),
+                       "r"(r[cc][4 * v + 3])
+                       : "memory");
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_reduce_add_3d(&tm_dq, sbase + Cfg::kdQ + slot, cc * 32, qt * 128, qh);
+          bulk_commit();
+        }
+      }
+    }
+    if (ok && GS > 1) {
+      // Group split: add the fp32 dV / dK partials the compute warps stage.
+      ok = named_bar_and(1, 128, mbar_wait_inl(bar_epi(0), 0, wc) &&
+                                     mbar_wait_inl(bar_epi(1), 0, wc));
+      if (ok && leader) {
+        for (int c = 0; c < D / 32; ++c) {
+          tma_reduce_add_3d(&tm_dv, sbase + Cfg::kQ0 + c * Cfg::kBox, c * 32, j * 128, bhkv);
+          tma_reduce_add_3d(&tm_dk, sbase + Cfg::kdO + c * Cfg::kBox, c * 32, j * 128, bhkv);
+        }
+        bulk_commit();
+      }
+    }
+    if (leader) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ compute warps 0-7
+    regs_increase<Cfg::kRegCompute>();
     const int wq = warp & 3;   // TMEM lane quadrant
-    const int ch = warp >> 2;  // column half
-    const int row = wq * 32 + lane;  // key row (dS, epilogue) / query row (dQ staging)
+    const int ch = warp >> 2;  // query half
+    const int row = wq * 32 + lane;  // key row
     const int kj = j * 128 + row;
     const bool key_live = kj < p.N;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -332,129 +394,125 @@ __global__ void __launch_bounds__(320, 1)
     const float2 c2 = make_float2(C, C);
     const uint32_t swz = (uint32_t)(row & 7);
     const uint32_t ds_row = sbase + Cfg::kdS + (uint32_t)ch * Cfg::kBox + (uint32_t)row * 128u;
+    const uint32_t ts = tS + lane_off + (uint32_t)ch * 64u;
+    const uint32_t tp = tdP + lane_off + (uint32_t)ch * 64u;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
-      // ---- dS = P o (dP - Delta) for queries [64ch, 64ch + 64) of this key row
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, (uint32_t)it & 1u, wc) &&
-                                       mbar_wait(bar_qd_full(s), (uint32_t)(it >> 1) & 1u, wc));
+      // ---- P = 2^(S c - LSE2) for queries [64ch, 64ch + 64) of this key row
+      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_s, (uint32_t)it & 1u, wc) &&
+                                       mbar_wait_inl(bar_q_full(s), (uint32_t)(it >> 1) & 1u, wc));
       if (!ok) break;
       tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kVec + s * 1024) + ch * 64;
       const float* delta = lse2 + 128;
       const bool diag = CAUSAL && q_tile(it) == j;
-      const uint32_t ts = tS + lane_off + (uint32_t)ch * 64u;
-      const uint32_t tp = tdP + lane_off + (uint32_t)ch * 64u;
-      uint32_t sr[2][16], dr[2][16];
-      tmem_ld16(ts, sr[0]);
-      tmem_ld16(tp, dr[0]);
+      float pf[64];
+      {
+        uint32_t sr[2][16];
+        tmem_ld16(ts, sr[0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 16 query columns per chunk, the next one in flight
-        const int bb = c & 1;
-        tmem_ld_wait();
-        if (c + 1 < 4) {
-          tmem_ld16(ts + (c + 1) * 16, sr[bb ^ 1]);
-          tmem_ld16(tp + (c + 1) * 16, dr[bb ^ 1]);
-        }
-        uint32_t pk[8], dk[8];
+        for (int c = 0; c < 4; ++c) {  // 16 query columns per chunk, the next one in flight
+          const int bb = c & 1;
+          tmem_ld_wait();
+          if (c + 1 < 4) tmem_ld16(ts + (c + 1) * 16, sr[bb ^ 1]);
+          uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const int qc = c * 16 + e;  // query within this half
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + qc);
-          const float4 d4 = *reinterpret_cast<const float4*>(delta + qc);
+          for (int e = 0; e < 16; e += 4) {
+            const int qc = c * 16 + e;  // query within this half
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + qc);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int ee = e + 2 * h;
-            const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-            const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-            const float2 x = __ffma2_rn(
-                make_float2(__uint_as_float(sr[bb][ee]), __uint_as_float(sr[bb][ee + 1])), c2, nl);
-            float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (diag) {  // causal: query < key is masked
-              const int q = ch * 64 + qc + 2 * h;
-              if (q < row) pp.x = 0.f;
-              if (q + 1 < row) pp.y = 0.f;
+            for (int h = 0; h < 2; ++h) {
+              const int ee = e + 2 * h;
+              const float2 nl = h ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+              const float2 x = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[bb][ee]), __uint_as_float(sr[bb][ee + 1])), c2,
+                  nl);
+              float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              if (diag) {  // causal: query < key is masked
+                const int q = ch * 64 + qc + 2 * h;
+                if (q < row) pp.x = 0.f;
+                if (q + 1 < row) pp.y = 0.f;
+              }
+              if (!key_live) pp = make_float2(0.f, 0.f);
+              pf[c * 16 + ee] = pp.x;
+              pf[c * 16 + ee + 1] = pp.y;
+              pk[ee / 2] = pack_bf16x2(pp.x, pp.y);
             }
-            if (!key_live) pp = make_float2(0.f, 0.f);
-            const float2 dd = __fadd2_rn(
-                make_float2(__uint_as_float(dr[bb][ee]), __uint_as_float(dr[bb][ee + 1])), nd);
-            const float2 ds = __fmul2_rn(pp, dd);
-            pk[ee / 2] = pack_bf16x2(pp.x, pp.y);
-            dk[ee / 2] = pack_bf16x2(ds.x, ds.y);
           }
-        }
-        // P^T (bf16) over S^T columns this warp has already read.
-        tmem_st8(ts + c * 8, pk);
-        // dS^T row to shared memory (box ch) in the 128-byte swizzled layout.
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-          const uint32_t chunk = ((uint32_t)(c * 2 + v)) ^ swz;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ds_row + chunk * 16),
-                       "r"(dk[4 * v]), "r"(dk[4 * v + 1]), "r"(dk[4 * v + 2]), "r"(dk[4 * v + 3])
-                       : "memory");
+          // P^T (bf16) over S^T columns this warp has already read.
+          tmem_st8(ts + c * 8, pk);
         }
       }
       tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+
+      // ---- dS = P o (dP - Delta) for the same queries, to shared memory
+      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_dp, (uint32_t)it & 1u, wc));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t dr[2][16];
+        tmem_ld16(tp, dr[0]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int bb = c & 1;
+          tmem_ld_wait();
+          if (c + 1 < 4) tmem_ld16(tp + (c + 1) * 16, dr[bb ^ 1]);
+          uint32_t dk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const int qc = c * 16 + e;
+            const float4 d4 = *reinterpret_cast<const float4*>(delta + qc);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int ee = e + 2 * h;
+              const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+              const float2 dd = __fadd2_rn(
+                  make_float2(__uint_as_float(dr[bb][ee]), __uint_as_float(dr[bb][ee + 1])), nd);
+              const float2 ds = __fmul2_rn(make_float2(pf[c * 16 + ee], pf[c * 16 + ee + 1]), dd);
+              dk[ee / 2] = pack_bf16x2(ds.x, ds.y);
+            }
+          }
+          // dS^T row to shared memory (box ch) in the 128-byte swizzled layout.
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const uint32_t chunk = ((uint32_t)(c * 2 + v)) ^ swz;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(ds_row + chunk * 16),
+                         "r"(dk[4 * v]), "r"(dk[4 * v + 1]), "r"(dk[4 * v + 2]), "r"(dk[4 * v + 3])
+                         : "memory");
+          }
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
-
-      // ---- dQ_it: TMEM -> registers -> stage `s` (all MMAs reading it are done)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, (uint32_t)it & 1u, wc));
-      if (!ok) break;
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_done, 0, wc));
+    if (ok && GS > 1) {
+      // Group split: stage this row's fp32 dV (half 0) or unscaled dK (half 1)
+      // partial for the dQ warpgroup's reduce-add.
       tc_fence_after();
-      uint32_t r[D / 64][32];  // this warp's D/2 dQ columns of its query row
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) tmem_ld32(tdP + lane_off + (ch * (D / 64) + cc) * 32, r[cc]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dq_free);
-      // Boxes of [128 rows x 32 fp32], 128-byte rows, 16-byte chunks swizzled by row & 7.
-      const uint32_t stage = sbase + Cfg::kQ0 + s * 2 * Cfg::kTile + (uint32_t)row * 128u;
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc)
+      const uint32_t src = (ch ? tdK : tdV) + lane_off;
+      const uint32_t stage = sbase + (ch ? Cfg::kdO : Cfg::kQ0) + (uint32_t)row * 128u;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(src + c * 32, rr);
+        tmem_ld_wait();
 #pragma unroll
         for (int v = 0; v < 8; ++v)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           stage + (ch * (D / 64) + cc) * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
-                       "r"(r[cc][4 * v]), "r"(r[cc][4 * v + 1]), "r"(r[cc][4 * v + 2]),
-                       "r"(r[cc][4 * v + 3])
+                           stage + c * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
+                       "r"(rr[4 * v]), "r"(rr[4 * v + 1]), "r"(rr[4 * v + 2]), "r"(rr[4 * v + 3])
                        : "memory");
+      }
       fence_proxy_async_smem();
-      if (it > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_red_go, (uint32_t)(it - 1) & 1u, wc));
-        if (!ok) break;
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_staged(ch));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, wc));
-    if (ok && GS > 1) {
-      // Group split: stage this row's fp32 dV (half 0) or unscaled dK (half 1)
-      // partial into ring stage `ch` for the producer's reduce-add.
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_prod_done, 0, wc));
-      if (ok) {
-        tc_fence_after();
-        const uint32_t src = (ch ? tdK : tdV) + lane_off;
-        const uint32_t stage = sbase + Cfg::kQ0 + ch * 2 * Cfg::kTile + (uint32_t)row * 128u;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(src + c * 32, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             stage + c * Cfg::kBox + ((((uint32_t)v) ^ swz) << 4)),
-                         "r"(rr[4 * v]), "r"(rr[4 * v + 1]), "r"(rr[4 * v + 2]), "r"(rr[4 * v + 3])
-                         : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_epi(ch));
-      }
+      if (lane == 0) mbar_arrive(bar_epi(ch));
     } else if (ok) {
       // Epilogue: half 0 writes dV, half 1 writes dK (scaled) of this key row.
       tc_fence_after();
@@ -484,7 +542,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);

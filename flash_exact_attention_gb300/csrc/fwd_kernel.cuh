@@ -63,6 +63,10 @@ struct FwdCfg {
   static constexpr int kNumBars = 1 + 2 * kStages + 5;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + misc + alignment slack
   static constexpr int kThreads = 384;
+  // Register split (per thread): 8 softmax warps, 4 other warps.
+  static constexpr int kRegSoftmax = 224, kRegOther = 56;
+  static_assert(8 * kRegSoftmax + 4 * kRegOther == 12 * launch_regs(kThreads),
+                "the register split must add up to the launch allocation");
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    regs_decrease<Cfg::kRegOther>();
     if (lane == 0) {
       const int nq = has_t1 ? 2 : 1;
       mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    regs_decrease<Cfg::kRegOther>();
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0);
       constexpr uint32_t kIdescO = make_idesc_bf16(128, D, 1);
@@ -252,10 +256,10 @@ __global__ void __launch_bounds__(384, 1)
       if (!ok) mbar_wait_drain_inl(bar_o(), 0, wc);
     }
   } else if (warp >= 10) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    regs_decrease<Cfg::kRegOther>();
   } else {
     // ------------------------------------------------------------ softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    regs_increase<Cfg::kRegSoftmax>();
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;

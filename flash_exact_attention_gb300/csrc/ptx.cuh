@@ -211,6 +211,38 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// As mma_ss / mma_ts, with each descriptor given as its address word plus a
+// K-step offset (added inside the asm, so the compiler keeps one register per
+// operand tile instead of hoisting every descriptor of a loop) and the common
+// high word.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_off,
+                                         uint32_t b_lo, uint32_t b_off, uint32_t hi,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+      "add.u32 al, %1, %2;\n\t"
+      "add.u32 bl, %3, %4;\n\t"
+      "mov.b64 ad, {al, %5};\n\t"
+      "mov.b64 bd, {bl, %5};\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %6, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_off), "r"(b_lo), "r"(b_off), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                         uint32_t b_off, uint32_t hi, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 bl;\n\t.reg .b64 bd;\n\t"
+      "add.u32 bl, %2, %3;\n\t"
+      "mov.b64 bd, {bl, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_off), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 ops of this
 // thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -238,6 +270,17 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46)  // descriptor version
          | (2ull << 61);                                           // 128-byte swizzle
+}
+
+// The same descriptor split in two 32-bit words (low: address and LBO; high:
+// SBO, version, swizzle), so that a kernel forms the low word once per tile and
+// adds a K-step offset with one 32-bit add: (addr >> 4) stays below 2^14 for any
+// shared-memory address, so the add never carries out of the address field.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
 // TMEM -> registers: 32 lanes x 32 consecutive 32-bit columns (one row per thread).
@@ -341,6 +384,41 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 // Barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier over a subset of the CTA's warps that also ANDs a predicate over
+// them: every participating thread gets the same answer.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------------ register split
+// Registers per thread a kernel of `threads` threads is launched with when it
+// asks for all of them (__launch_bounds__(threads, 1)): the register file
+// divided evenly, rounded down to the allocation granularity of 8.
+constexpr int launch_regs(int threads) { return (65536 / threads) / 8 * 8; }
+
+// setmaxnreg: the whole warpgroup moves to R registers per thread.  An
+// increase waits until other warpgroups have released enough, so the kernels
+// check with static_asserts that their split adds up to the launch allocation.
+template <int R>
+__device__ __forceinline__ void regs_increase() {
+  static_assert(R % 8 == 0 && R >= 24 && R <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R) : "memory");
+}
+template <int R>
+__device__ __forceinline__ void regs_decrease() {
+  static_assert(R % 8 == 0 && R >= 24 && R <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R) : "memory");
 }
 
 // ------------------------------------------------------------------ math
