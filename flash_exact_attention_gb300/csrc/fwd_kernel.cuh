@@ -187,19 +187,25 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t tS[2] = {tmem_base, tmem_base + 128};
       const uint32_t tO[2] = {tmem_base + 256, tmem_base + 384};
       auto ring = [&](int s) { return sbase + Cfg::kRingOff + s * Cfg::kTileBytes; };
+      // Descriptors as an address word per tile plus a K-step offset added inside
+      // the MMA's asm (one register per tile; nothing hoisted per K step).
+      constexpr uint32_t kHi = sdesc_sw128_hi(1024);
+      const uint32_t q_lo[2] = {sdesc_sw128_lo(q_addr[0], 16), sdesc_sw128_lo(q_addr[1], 16)};
+      auto koff = [](int kk) {  // K-major: 32-byte steps inside a 64-column box, then a box
+        return (uint32_t)(((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4);
+      };
       auto issue_qk = [&](int t, uint32_t kaddr) {
+        const uint32_t k_lo = sdesc_sw128_lo(kaddr, 16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32;
-          mma_ss(tS[t], make_sdesc_sw128(q_addr[t] + off, 16, 1024),
-                 make_sdesc_sw128(kaddr + off, 16, 1024), kIdescS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_w(tS[t], q_lo[t], koff(kk), k_lo, koff(kk), kHi, kIdescS, kk > 0);
       };
       auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+        const uint32_t v_lo = sdesc_sw128_lo(vaddr, Cfg::kBoxBytes);  // MN-major: 16 rows per step
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO[t], tS[t] + kk * 8, make_sdesc_sw128(vaddr + kk * 2048, Cfg::kBoxBytes, 1024),
-                 kIdescO, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_w(tO[t], tS[t] + kk * 8, v_lo, (uint32_t)((kk * 2048) >> 4), kHi, kIdescO,
+                   (acc || kk > 0) ? 1u : 0u);
       };
 
       bool ok = mbar_wait_inl(bar_q(), 0, wc);
