@@ -50,8 +50,8 @@
 //
 // TMEM columns: [0,128) S^T, with P^T (bf16) of queries 0-63 written over
 // columns [0,32) and of queries 64-127 over [64,96) (each half stays inside the
-// S^T columns its own warps read); [128,256) dP^T, later overwritten by dQ_i;
-// [256,256+D) dV; [256+D,256+2D) dK.
+// S^T columns its own warps read); [128,256) dP^T; [256,256+D) dV;
+// [256+D,256+2D) dK; dQ_i at [256+2D,256+3D) when D=64, else over dP^T.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -186,8 +186,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     return CAUSAL ? i0 + r : (r + j) % T;
   };
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
+  // At D=64 dQ has columns of its own, so dP_{it+1} need not wait for dQ_it to
+  // be read out; at D=128 the 512 columns are full and dQ reuses dP's.
+  constexpr bool kOwnDq = 256 + 3 * D <= (int)Cfg::kTmemCols;
   const uint32_t tS = tmem_base, tdP = tmem_base + 128, tdV = tmem_base + 256,
-                 tdK = tmem_base + 256 + D;
+                 tdK = tmem_base + 256 + D, tdQ = kOwnDq ? tmem_base + 256 + 2 * D : tdP;
 
   if (warp >= 12) {
     regs_decrease<Cfg::kRegOther>();
@@ -275,7 +278,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         constexpr int s = decltype(stage)::value;
         const uint32_t mQs_ = mQ0 + s * kQs, kQn = kQ0 + (s ^ 1) * kQs;
         // dP_it over the dP^T columns, once dQ_{it-1} has been read out of them.
-        if (it > 0 && !mbar_wait_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc)) return false;
+        if (!kOwnDq && it > 0 && !mbar_wait_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
+          return false;
         if (!mbar_wait_inl(bar_do_full, (uint32_t)it & 1u, wc)) return false;
         tc_fence_after();
         issue_t(tdP, kV, kdO);
@@ -303,9 +307,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss_w(tdK, kdS, koff(kk), mQs_, moff(kk), kHi, kIdescB_MN,
                    (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar_q_free(s));
+        if (kOwnDq && it > 0 && !mbar_wait_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
+          return false;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys), into the dP^T columns
-          mma_ss_w(tdP, mdS, moff(kk), mK, moff(kk), kHi, kIdescDQ, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys)
+          mma_ss_w(tdQ, mdS, moff(kk), mK, moff(kk), kHi, kIdescDQ, kk > 0);
         mma_commit(bar_dq);
         return true;
       };
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_after();
       uint32_t r[D / 32][32];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tdP + lane_off + cc * 32, r[cc]);
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tdQ + lane_off + cc * 32, r[cc]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -454,13 +460,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       {
-        uint32_t dr[2][16];
-        tmem_ld16(tp, dr[0]);
+        // All 64 dP columns in one round trip (one wait instead of four).
+        uint32_t dra[32], drb[32];
+        tmem_ld32(tp, dra);
+        tmem_ld32(tp + 32, drb);
+        tmem_ld_wait();
+        auto dpv = [&](int q) { return __uint_as_float(q < 32 ? dra[q] : drb[q - 32]); };
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int bb = c & 1;
-          tmem_ld_wait();
-          if (c + 1 < 4) tmem_ld16(tp + (c + 1) * 16, dr[bb ^ 1]);
           uint32_t dk[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {
@@ -470,8 +477,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             for (int h = 0; h < 2; ++h) {
               const int ee = e + 2 * h;
               const float2 nd = h ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-              const float2 dd = __fadd2_rn(
-                  make_float2(__uint_as_float(dr[bb][ee]), __uint_as_float(dr[bb][ee + 1])), nd);
+              const float2 dd =
+                  __fadd2_rn(make_float2(dpv(c * 16 + ee), dpv(c * 16 + ee + 1)), nd);
               const float2 ds = __fmul2_rn(make_float2(pf[c * 16 + ee], pf[c * 16 + ee + 1]), dd);
               dk[ee / 2] = pack_bf16x2(ds.x, ds.y);
             }
