@@ -225,12 +225,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       bool ok = true;
       for (int it = 0; it < n_it && ok; ++it) {
         if (it + 1 < n_it) {
-          if (!(ok = mbar_wait_inl(bar_do_free, (uint32_t)it & 1u, wc))) break;
+          if (!(ok = mbar_wait_tested_inl(bar_do_free, (uint32_t)it & 1u, wc))) break;
           load_do(it + 1);
           ++ndo;
         }
         if (it + 2 < n_it) {
-          if (!(ok = mbar_wait_inl(bar_q_free(it & 1), (uint32_t)(it >> 1) & 1u, wc))) break;
+          if (!(ok = mbar_wait_tested_inl(bar_q_free(it & 1), (uint32_t)(it >> 1) & 1u, wc))) break;
           load_q(it + 2);
           ++nq;
         }
@@ -278,14 +278,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         constexpr int s = decltype(stage)::value;
         const uint32_t mQs_ = mQ0 + s * kQs, kQn = kQ0 + (s ^ 1) * kQs;
         // dP_it over the dP^T columns, once dQ_{it-1} has been read out of them.
-        if (!kOwnDq && it > 0 && !mbar_wait_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
+        if (!mbar_wait_tested_inl(bar_do_full, (uint32_t)it & 1u, wc)) return false;
+        if (!kOwnDq && it > 0 && !mbar_wait_tested_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
           return false;
-        if (!mbar_wait_inl(bar_do_full, (uint32_t)it & 1u, wc)) return false;
         tc_fence_after();
         issue_t(tdP, kV, kdO);
         mma_commit(bar_dp);
         // dV += P^T dO  (K = 128 queries; A = P^T from TMEM)
-        if (!mbar_wait_inl(bar_p, (uint32_t)it & 1u, wc)) return false;
+        if (!mbar_wait_tested_inl(bar_p, (uint32_t)it & 1u, wc)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -294,12 +294,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit(bar_do_free);
         // S_{it+1} over the S^T columns (P^T_it has been consumed by dV, in order).
         if (it + 1 < n_it) {
-          if (!mbar_wait_inl(bar_q_full(s ^ 1), (uint32_t)((it + 1) >> 1) & 1u, wc)) return false;
+          if (!mbar_wait_tested_inl(bar_q_full(s ^ 1), (uint32_t)((it + 1) >> 1) & 1u, wc)) return false;
           tc_fence_after();
           issue_t(tS, kK, kQn);
           mma_commit(bar_s);
         }
-        if (!mbar_wait_inl(bar_ds, (uint32_t)it & 1u, wc)) return false;
+        if (!mbar_wait_tested_inl(bar_ds, (uint32_t)it & 1u, wc)) return false;
         tc_fence_after();
         // dK += dS^T Q first: it frees Q stage s for the producer one MMA group earlier.
 #pragma unroll
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss_w(tdK, kdS, koff(kk), mQs_, moff(kk), kHi, kIdescB_MN,
                    (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar_q_free(s));
-        if (kOwnDq && it > 0 && !mbar_wait_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
+        if (kOwnDq && it > 0 && !mbar_wait_tested_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
           return false;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys)
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit(bar_dq);
         return true;
       };
-      bool ok = mbar_wait_inl(bar_kv, 0, wc) && mbar_wait_inl(bar_q_full(0), 0, wc);
+      bool ok = mbar_wait_tested_inl(bar_kv, 0, wc) && mbar_wait_tested_inl(bar_q_full(0), 0, wc);
       if (ok) {
         tc_fence_after();
         issue_t(tS, kK, kQ0);
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       // One decision for the whole warpgroup: its named barriers need all 4 warps.
-      ok = named_bar_and(1, 128, mbar_wait_inl(bar_dq, (uint32_t)it & 1u, wc));
+      ok = named_bar_and(1, 128, mbar_wait_tested_inl(bar_dq, (uint32_t)it & 1u, wc));
       if (!ok) break;
       tc_fence_after();
       uint32_t r[D / 32][32];
@@ -376,8 +376,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     if (ok && GS > 1) {
       // Group split: add the fp32 dV / dK partials the compute warps stage.
-      ok = named_bar_and(1, 128, mbar_wait_inl(bar_epi(0), 0, wc) &&
-                                     mbar_wait_inl(bar_epi(1), 0, wc));
+      ok = named_bar_and(1, 128, mbar_wait_tested_inl(bar_epi(0), 0, wc) &&
+                                     mbar_wait_tested_inl(bar_epi(1), 0, wc));
       if (ok && leader) {
         for (int c = 0; c < D / 32; ++c) {
           tma_reduce_add_3d(&tm_dv, sbase + Cfg::kQ0 + c * Cfg::kBox, c * 32, j * 128, bhkv);
@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       // ---- P = 2^(S c - LSE2) for queries [64ch, 64ch + 64) of this key row
-      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_s, (uint32_t)it & 1u, wc) &&
-                                       mbar_wait_inl(bar_q_full(s), (uint32_t)(it >> 1) & 1u, wc));
+      ok = __all_sync(0xffffffffu, mbar_wait_tested_inl(bar_s, (uint32_t)it & 1u, wc) &&
+                                       mbar_wait_tested_inl(bar_q_full(s), (uint32_t)(it >> 1) & 1u, wc));
       if (!ok) break;
       tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(smem + Cfg::kVec + s * 1024) + ch * 64;
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (lane == 0) mbar_arrive(bar_p);
 
       // ---- dS = P o (dP - Delta) for the same queries, to shared memory
-      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_dp, (uint32_t)it & 1u, wc));
+      ok = __all_sync(0xffffffffu, mbar_wait_tested_inl(bar_dp, (uint32_t)it & 1u, wc));
       if (!ok) break;
       tc_fence_after();
       {
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_done, 0, wc));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_tested_inl(bar_done, 0, wc));
     if (ok && GS > 1) {
       // Group split: stage this row's fp32 dV (half 0) or unscaled dK (half 1)
       // partial for the dQ warpgroup's reduce-add.
