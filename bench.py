@@ -280,7 +280,10 @@ def run_native(args):
     fwd_tflops = ff / (ms_fwd_launch * 1e-3) / 1e12
     bwd_tflops = 2.5 * ff / (ms_bwd_call * 1e-3) / 1e12 if has_bwd else None
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    # ---- end to end through the C ABI from pinned host buffers: every step copies
+    # its inputs in and its results out.  As a training or serving loop would, the
+    # copies run on their own streams (host->device and device->host engines) and
+    # overlap the neighbouring steps' kernels, with two device buffer sets.
     out_names = ["o", "lse"] + (["dq", "dk", "dv"] if has_bwd else [])
     outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
     host_out = {n: torch.empty(outs[n].shape, dtype=outs[n].dtype, pin_memory=True)
@@ -289,19 +292,63 @@ def run_native(args):
     h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
     d2h = sum(host_out[n].numel() * host_out[n].element_size() for n in out_names)
     e2e_steps = max(3, min(args.steps, 20))
-    barrier()
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for _ in range(e2e_steps):
-        for n in in_names:
-            dev[n].copy_(host[n], non_blocking=True)
-        step()
-        for n in out_names:
-            host_out[n].copy_(outs[n], non_blocking=True)
-    g1.record(stream)
-    barrier()
-    ms_e2e = g0.elapsed_time(g1) / e2e_steps
+    bufs = [dict(dev, **outs), {n: torch.empty_like(t) for n, t in dict(dev, **outs).items()}]
+
+    # Three streams of their own (none is the legacy default stream, which would
+    # serialise with the others).
+    comp_stream, h2d_stream, d2h_stream = (torch.cuda.Stream(), torch.cuda.Stream(),
+                                           torch.cuda.Stream())
+    csh = comp_stream.cuda_stream
+
+    def step_on(b):
+        st = binding.attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], B, Hq, Hkv, N, D, causal,
+                              scale, csh)
+        if st:
+            raise binding.AttnError(st, "attn_fwd")
+        if has_bwd:
+            st = binding.attn_bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], B, Hq, Hkv, N, D,
+                                  causal, scale, csh, b["do"], b["dq"], b["dk"], b["dv"])
+            if st:
+                raise binding.AttnError(st, "attn_bwd")
+
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    def e2e_pass():
+        """e2e_steps pipelined steps; returns ms per step (CUDA events)."""
+        barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(comp_stream)
+        h2d_stream.wait_event(g0)
+        for i in range(e2e_steps):
+            b = i % 2
+            with torch.cuda.stream(h2d_stream):
+                if i >= 2:
+                    h2d_stream.wait_event(ev_comp[b])  # step i-2 is done reading set b
+                for n in in_names:
+                    bufs[b][n].copy_(host[n], non_blocking=True)
+                ev_in[b].record(h2d_stream)
+            comp_stream.wait_event(ev_in[b])
+            if i >= 2:
+                comp_stream.wait_event(ev_out[b])  # step i-2's results in set b are copied out
+            step_on(bufs[b])
+            ev_comp[b].record(comp_stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(ev_comp[b])
+                for n in out_names:
+                    host_out[n].copy_(bufs[b][n], non_blocking=True)
+                ev_out[b].record(d2h_stream)
+        g1.record(d2h_stream)
+        barrier()
+        return g0.elapsed_time(g1) / e2e_steps
+
+    e2e_pass()  # untimed: first use of the second buffer set and of the host buffers
+    e2e_runs = sorted(e2e_pass() for _ in range(3))
+    ms_e2e = e2e_runs[1]  # median of three timed passes
+    st = binding.attn_device_status(csh)
+    if st:
+        raise binding.AttnError(st, "end-to-end leg")
     ms_e2e = max_over_ranks([ms_e2e], dist, "cuda")[0]
     e2e_value = job_tflops(ws, step_flops, ms_e2e)
 
@@ -343,6 +390,8 @@ def run_native(args):
         "roofline": roofline,
         "roofline_fwd": roof_fwd,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "overlap": "copies on their own streams, two device buffer sets",
+                "passes_ms_per_step": [round(x, 4) for x in e2e_runs],
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
