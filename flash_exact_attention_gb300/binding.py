@@ -166,3 +166,42 @@ def flash_attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, stream=None)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+_ATTN_FUNCTION = None
+
+
+def _attn_function():
+    """torch.autograd.Function over attn_fwd / attn_bwd (built on first use so
+    that importing this module does not import torch)."""
+    global _ATTN_FUNCTION
+    if _ATTN_FUNCTION is None:
+        import torch
+
+        class AttnFunction(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, causal, scale):
+                o, lse = flash_attn(q, k, v, causal=causal, scale=scale)
+                ctx.save_for_backward(q, k, v, o, lse)
+                ctx.causal, ctx.scale = causal, scale
+                ctx.mark_non_differentiable(lse)
+                return o, lse
+
+            @staticmethod
+            def backward(ctx, dout, dlse):
+                q, k, v, o, lse = ctx.saved_tensors
+                dq, dk, dv = flash_attn_bwd(q, k, v, o, lse, dout.contiguous(),
+                                            causal=ctx.causal, scale=ctx.scale)
+                return dq, dk, dv, None, None
+
+        _ATTN_FUNCTION = AttnFunction
+    return _ATTN_FUNCTION
+
+
+def attention(q, k, v, causal=False, scale=None):
+    """Differentiable O = softmax(scale q k^T) v for bf16 CUDA tensors q [B,Hq,N,D],
+    k/v [B,Hkv,N,D]: the forward is attn_fwd, the gradient attn_bwd (on torch's
+    current stream).  Returns O; the row log-sum-exp is kept for the backward."""
+    o, _ = _attn_function().apply(q, k, v, bool(causal),
+                                  1.0 / math.sqrt(q.shape[-1]) if scale is None else scale)
+    return o
