@@ -28,6 +28,8 @@ SIGNATURES = {
     "attn_bwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
     "attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P],
                          _I),
+    "attn_fwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_bwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
     "attn_bwd_noalloc_scratch_limit": ([], ctypes.c_longlong),
     "attn_status_string": ([_I], ctypes.c_char_p),
     "attn_device_status": ([_P], _I),
@@ -96,6 +98,19 @@ def attn_bwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq,
                            _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
 
 
+def attn_fwd_f16(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream=None):
+    """Raw call, fp16 tensors: pointers (ints) or tensors; returns the status code."""
+    return load().attn_fwd_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D,
+                               int(bool(causal)), float(scale), _stream_handle(stream))
+
+
+def attn_bwd_f16(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk, dv):
+    """Raw call, fp16 tensors: pointers (ints) or tensors; returns the status code."""
+    return load().attn_bwd_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D,
+                               int(bool(causal)), float(scale), _stream_handle(stream),
+                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
+
+
 def attn_bwd_noalloc(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
                      dv):
     """Raw call of the backward that allocates nothing (fixed scratch array)."""
@@ -122,27 +137,31 @@ def attn_set_wait_timeout_ms(ms):
 
 
 # ------------------------------------------------------- tensor conveniences
-def _check(t, shape, name):
+def _check(t, shape, name, dtype=None):
     import torch
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError("%s must be a contiguous CUDA bf16 tensor" % name)
+    if dtype is None:
+        dtype = t.dtype
+    if dtype not in (torch.bfloat16, torch.float16) or t.dtype != dtype or not t.is_cuda or \
+            not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor of q's dtype (bf16 or fp16)" % name)
     if tuple(t.shape) != tuple(shape):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
 
 
 def flash_attn(q, k, v, causal=False, scale=None, stream=None):
-    """O, LSE = attention(q, k, v); q [B,Hq,N,D], k/v [B,Hkv,N,D] bf16 on CUDA."""
+    """O, LSE = attention(q, k, v); q [B,Hq,N,D], k/v [B,Hkv,N,D] bf16 or fp16 on CUDA."""
     import torch
     B, Hq, N, D = q.shape
     Hkv = k.shape[1]
     _check(q, (B, Hq, N, D), "q")
-    _check(k, (B, Hkv, N, D), "k")
-    _check(v, (B, Hkv, N, D), "v")
+    _check(k, (B, Hkv, N, D), "k", q.dtype)
+    _check(v, (B, Hkv, N, D), "v", q.dtype)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    st = attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream)
+    call = attn_fwd_f16 if q.dtype == torch.float16 else attn_fwd
+    st = call(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
     return o, lse
@@ -156,13 +175,14 @@ def flash_attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, stream=None)
     for t, shp, nm in ((q, (B, Hq, N, D), "q"), (k, (B, Hkv, N, D), "k"),
                        (v, (B, Hkv, N, D), "v"), (o, (B, Hq, N, D), "o"),
                        (dout, (B, Hq, N, D), "dout")):
-        _check(t, shp, nm)
+        _check(t, shp, nm, q.dtype)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    st = attn_bwd(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk, dv)
+    call = attn_bwd_f16 if q.dtype == torch.float16 else attn_bwd
+    st = call(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk, dv)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
@@ -199,7 +219,7 @@ def _attn_function():
 
 
 def attention(q, k, v, causal=False, scale=None):
-    """Differentiable O = softmax(scale q k^T) v for bf16 CUDA tensors q [B,Hq,N,D],
+    """Differentiable O = softmax(scale q k^T) v for bf16 or fp16 CUDA tensors q [B,Hq,N,D],
     k/v [B,Hkv,N,D]: the forward is attn_fwd, the gradient attn_bwd (on torch's
     current stream).  Returns O; the row log-sum-exp is kept for the backward."""
     o, _ = _attn_function().apply(q, k, v, bool(causal),

@@ -84,15 +84,16 @@ int device_sm_count(int dev) {
   return (dev >= 0 && dev < kMaxDevices) ? g_num_sms[dev] : 0;
 }
 
-// 3-D map over a contiguous bf16 [BH, N, D] tensor: dims (D, N, BH), box
+// 3-D map over a contiguous bf16 (or fp16) [BH, N, D] tensor: dims (D, N, BH), box
 // (64, 128, 1), 128-byte swizzle.  Rows past N inside a (batch, head) plane
 // read as zero, so a ragged tail never reads the next head.
-int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
+int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16) {
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -129,7 +130,7 @@ int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale) {
 
 
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-              int Hkv, int N, int D, int causal, float scale, void* stream) {
+              int Hkv, int N, int D, int causal, float scale, void* stream, bool f16) {
   int st = validate_shape(B, Hq, Hkv, N, D, scale);
   if (st != ATTN_OK) return st;
   if ((long long)B * Hq * N == 0) return ATTN_OK;
@@ -142,9 +143,9 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (st != ATTN_OK) return st;
 
   CUtensorMap tq, tk, tv;
-  if (encode_tile_map(&tq, q, D, N, B * Hq) != ATTN_OK ||
-      encode_tile_map(&tk, k, D, N, B * Hkv) != ATTN_OK ||
-      encode_tile_map(&tv, v, D, N, B * Hkv) != ATTN_OK)
+  if (encode_tile_map(&tq, q, D, N, B * Hq, f16) != ATTN_OK ||
+      encode_tile_map(&tk, k, D, N, B * Hkv, f16) != ATTN_OK ||
+      encode_tile_map(&tv, v, D, N, B * Hkv, f16) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   FwdParams p;
@@ -164,8 +165,11 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.timeout_ns = wait_timeout_ns();
   p.err = err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (D == 64) ? launch_fwd_d64(tq, tk, tv, p, causal != 0, s)
-                            : launch_fwd_d128(tq, tk, tv, p, causal != 0, s);
+  const bool c = causal != 0;
+  cudaError_t e = f16 ? ((D == 64) ? launch_fwd_d64_f16(tq, tk, tv, p, c, s)
+                                   : launch_fwd_d128_f16(tq, tk, tv, p, c, s))
+                      : ((D == 64) ? launch_fwd_d64(tq, tk, tv, p, c, s)
+                                   : launch_fwd_d128(tq, tk, tv, p, c, s));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -205,6 +209,18 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              const void* dout, void* dq, void* dk, void* dv) {
   return attn::bwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
                          dv);
+}
+
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int N, int D, int causal, float scale, void* stream) {
+  return attn::fwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, true);
+}
+
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 int B, int Hq, int Hkv, int N, int D, int causal, float scale, void* stream,
+                 const void* dout, void* dq, void* dk, void* dv) {
+  return attn::bwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
+                         dv, true);
 }
 
 const char* attn_status_string(int status) {

@@ -46,7 +46,7 @@ int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, int B, int Hq, int Hkv, int N, int D, float scale,
                        const void* dout, void* dq, void* dk, void* dv, BwdParams* p,
                        CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tdo,
-                       bool allow_split) {
+                       bool allow_split, bool f16) {
   int st = validate_shape(B, Hq, Hkv, N, D, scale);
   if (st != ATTN_OK) return st;
   if ((long long)B * Hq * N == 0) return -1;  // nothing to do
@@ -57,10 +57,10 @@ int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
   unsigned int* err = nullptr;
   st = device_setup(&dev, &err);
   if (st != ATTN_OK) return st;
-  if (encode_tile_map(tq, q, D, N, B * Hq) != ATTN_OK ||
-      encode_tile_map(tk, k, D, N, B * Hkv) != ATTN_OK ||
-      encode_tile_map(tv, v, D, N, B * Hkv) != ATTN_OK ||
-      encode_tile_map(tdo, dout, D, N, B * Hq) != ATTN_OK)
+  if (encode_tile_map(tq, q, D, N, B * Hq, f16) != ATTN_OK ||
+      encode_tile_map(tk, k, D, N, B * Hkv, f16) != ATTN_OK ||
+      encode_tile_map(tv, v, D, N, B * Hkv, f16) != ATTN_OK ||
+      encode_tile_map(tdo, dout, D, N, B * Hq, f16) != ATTN_OK)
     return ATTN_ERR_CUDA;
   p->dk = dk;
   p->dv = dv;
@@ -97,19 +97,23 @@ int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
 
 int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
-                      const float* lse, void* dq, int D, int causal, cudaStream_t s) {
-  cudaError_t e = (D == 64) ? launch_bwd_d64(tq, tk, tv, tdo, p, o, dout, lse, dq, causal != 0, s)
-                            : launch_bwd_d128(tq, tk, tv, tdo, p, o, dout, lse, dq, causal != 0, s);
+                      const float* lse, void* dq, int D, int causal, cudaStream_t s, bool f16) {
+  const bool c = causal != 0;
+  cudaError_t e =
+      f16 ? ((D == 64) ? launch_bwd_d64_f16(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s)
+                       : launch_bwd_d128_f16(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s))
+          : ((D == 64) ? launch_bwd_d64(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s)
+                       : launch_bwd_d128(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
               int Hq, int Hkv, int N, int D, int causal, float scale, void* stream,
-              const void* dout, void* dq, void* dk, void* dv) {
+              const void* dout, void* dq, void* dk, void* dv, bool f16) {
   BwdParams p;
   CUtensorMap tq, tk, tv, tdo;
   int st = bwd_prepare(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, dout, dq, dk, dv, &p, &tq, &tk,
-                       &tv, &tdo, /*allow_split=*/true);
+                       &tv, &tdo, /*allow_split=*/true, f16);
   if (st == -1) return ATTN_OK;
   if (st != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -122,7 +126,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   p.delta = sc.delta;
   p.dk_acc = sc.dk_acc;
   p.dv_acc = sc.dv_acc;
-  st = bwd_launch(tq, tk, tv, tdo, p, o, dout, lse, dq, D, causal, s);
+  st = bwd_launch(tq, tk, tv, tdo, p, o, dout, lse, dq, D, causal, s, f16);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == ATTN_OK) st = ATTN_ERR_CUDA;
   return st;
 }

@@ -1,12 +1,12 @@
-// Backward kernels for head dim 64 (causal and non-causal).
+// Backward kernels for head dim 64, bf16 inputs and gradients (causal and non-causal).
 #include "bwd_launch.cuh"
 
 namespace attn {
 cudaError_t launch_bwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdParams& p, const void* o,
-                           const void* dout, const float* lse, void* dq, bool causal,
-                           cudaStream_t stream) {
-  return causal ? launch_bwd_impl<64, true>(tq, tk, tv, tdo, p, o, dout, lse, dq, stream)
-                : launch_bwd_impl<64, false>(tq, tk, tv, tdo, p, o, dout, lse, dq, stream);
+                          const CUtensorMap& tdo, const BwdParams& p, const void* o,
+                          const void* dout, const float* lse, void* dq, bool causal,
+                          cudaStream_t stream) {
+  return causal ? launch_bwd_impl<64, true, false>(tq, tk, tv, tdo, p, o, dout, lse, dq, stream)
+                : launch_bwd_impl<64, false, false>(tq, tk, tv, tdo, p, o, dout, lse, dq, stream);
 }
 }  // namespace attn

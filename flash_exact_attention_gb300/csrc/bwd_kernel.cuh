@@ -94,7 +94,7 @@ struct BwdCfg {
   static_assert(kTile + 2 * kBox >= (D / 32) * kBox, "dK partial staging");
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -244,9 +244,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
     } else if (warp == 13 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t kIdescB_MN = make_idesc_bf16(128, D, 1, 0);  // dV, dK
-      constexpr uint32_t kIdescDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A and B MN-major
+      constexpr uint32_t kIdescSS = make_idesc_bf16(128, 128, 0, 0, F16);
+      constexpr uint32_t kIdescB_MN = make_idesc_bf16(128, D, 1, 0, F16);  // dV, dK
+      constexpr uint32_t kIdescDQ = make_idesc_bf16(128, D, 1, 1, F16);    // dQ: A, B MN-major
       constexpr uint32_t kHi = sdesc_sw128_hi(1024);  // 8-row groups 1024 bytes apart
       // Address words of every operand, K-major (K advances inside a 128-byte
       // row, then by a 64-column box) or MN-major (K advances by 16 rows; the
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               if (!key_live) pp = make_float2(0.f, 0.f);
               pf[c * 16 + ee] = pp.x;
               pf[c * 16 + ee + 1] = pp.y;
-              pk[ee / 2] = pack_bf16x2(pp.x, pp.y);
+              pk[ee / 2] = pack2<F16>(pp.x, pp.y);
             }
           }
           // P^T (bf16) over S^T columns this warp has already read.
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               const float2 dd =
                   __fadd2_rn(make_float2(dpv(c * 16 + ee), dpv(c * 16 + ee + 1)), nd);
               const float2 ds = __fmul2_rn(make_float2(pf[c * 16 + ee], pf[c * 16 + ee + 1]), dd);
-              dk[ee / 2] = pack_bf16x2(ds.x, ds.y);
+              dk[ee / 2] = pack2<F16>(ds.x, ds.y);
             }
           }
           // dS^T row to shared memory (box ch) in the 128-byte swizzled layout.
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // Epilogue: half 0 writes dV, half 1 writes dK (scaled) of this key row.
       tc_fence_after();
       const size_t orow = ((size_t)bhkv * p.N + (size_t)(key_live ? kj : 0)) * D;
-      uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(ch ? p.dk : p.dv) + orow);
+      uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ch ? p.dk : p.dv) + orow);
       const float mul = ch ? p.scale : 1.f;
       const uint32_t src = (ch ? tdK : tdV) + lane_off;
 #pragma unroll
@@ -536,10 +536,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(rr[8 * v + 0]) * mul, __uint_as_float(rr[8 * v + 1]) * mul);
-            w.y = pack_bf16x2(__uint_as_float(rr[8 * v + 2]) * mul, __uint_as_float(rr[8 * v + 3]) * mul);
-            w.z = pack_bf16x2(__uint_as_float(rr[8 * v + 4]) * mul, __uint_as_float(rr[8 * v + 5]) * mul);
-            w.w = pack_bf16x2(__uint_as_float(rr[8 * v + 6]) * mul, __uint_as_float(rr[8 * v + 7]) * mul);
+            w.x = pack2<F16>(__uint_as_float(rr[8 * v + 0]) * mul, __uint_as_float(rr[8 * v + 1]) * mul);
+            w.y = pack2<F16>(__uint_as_float(rr[8 * v + 2]) * mul, __uint_as_float(rr[8 * v + 3]) * mul);
+            w.z = pack2<F16>(__uint_as_float(rr[8 * v + 4]) * mul, __uint_as_float(rr[8 * v + 5]) * mul);
+            w.w = pack2<F16>(__uint_as_float(rr[8 * v + 6]) * mul, __uint_as_float(rr[8 * v + 7]) * mul);
             out[c * 4 + v] = w;
           }
         }
@@ -558,9 +558,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
 // Delta and LSE2 into row-padded buffers; zero the dQ accumulator.  One warp per
 // padded row (b*Hq + h, i), i < Npad.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256)
-    bwd_preprocess(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+    bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                    const float* __restrict__ lse, float* __restrict__ lse2,
                    float* __restrict__ delta, float* __restrict__ dq_acc, long long rows, int N,
                    int Npad, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
@@ -575,18 +575,15 @@ __global__ void __launch_bounds__(256)
     constexpr int kPer = D / 32;  // elements per lane: 2 or 4
     const size_t base = ((size_t)bh * N + i) * D + (size_t)lane * kPer;
     if (kPer == 2) {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + base);
-      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dout + base);
-      acc = __bfloat162float(a.x) * __bfloat162float(g.x) + __bfloat162float(a.y) * __bfloat162float(g.y);
+      const float2 a = unpack2<F16>(*reinterpret_cast<const uint32_t*>(o + base));
+      const float2 g = unpack2<F16>(*reinterpret_cast<const uint32_t*>(dout + base));
+      acc = a.x * g.x + a.y * g.y;
     } else {
       const uint2 a = *reinterpret_cast<const uint2*>(o + base);
       const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        acc += __bfloat162float(a2[t].x) * __bfloat162float(g2[t].x) +
-               __bfloat162float(a2[t].y) * __bfloat162float(g2[t].y);
+      const float2 a0 = unpack2<F16>(a.x), a1 = unpack2<F16>(a.y);
+      const float2 g0 = unpack2<F16>(g.x), g1 = unpack2<F16>(g.y);
+      acc = a0.x * g0.x + a0.y * g0.y + a1.x * g1.x + a1.y * g1.y;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -610,9 +607,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // dQ = scale * dQacc (rows < N) -> bf16.  8 elements per thread.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256)
-    bwd_postprocess(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+    bwd_postprocess(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq,
                     long long rows, int N, int Npad, float scale) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element group
   constexpr int kGroups = D / 8;
@@ -624,19 +621,19 @@ __global__ void __launch_bounds__(256)
   const float4* src = reinterpret_cast<const float4*>(dq_acc + ((size_t)bh * Npad + i) * D + g * 8);
   const float4 a = src[0], c = src[1];
   uint4 w;
-  w.x = pack_bf16x2(a.x * scale, a.y * scale);
-  w.y = pack_bf16x2(a.z * scale, a.w * scale);
-  w.z = pack_bf16x2(c.x * scale, c.y * scale);
-  w.w = pack_bf16x2(c.z * scale, c.w * scale);
+  w.x = pack2<F16>(a.x * scale, a.y * scale);
+  w.y = pack2<F16>(a.z * scale, a.w * scale);
+  w.z = pack2<F16>(c.x * scale, c.y * scale);
+  w.w = pack2<F16>(c.z * scale, c.w * scale);
   reinterpret_cast<uint4*>(dq + (size_t)r * D)[g] = w;
 }
 
 // Group split: dK = scale * dKacc, dV = dVacc (rows < N) -> bf16.  8 elements
 // per thread; rows are (b*Hkv + h)*N + i.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(256)
     bwd_post_kv(const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
-                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, long long rows,
+                uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, long long rows,
                 int N, int Npad, float scale) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   constexpr int kGroups = D / 8;
@@ -652,10 +649,10 @@ __global__ void __launch_bounds__(256)
     const float m = which ? scale : 1.f;
     const float4 a = src[0], c = src[1];
     uint4 w;
-    w.x = pack_bf16x2(a.x * m, a.y * m);
-    w.y = pack_bf16x2(a.z * m, a.w * m);
-    w.z = pack_bf16x2(c.x * m, c.y * m);
-    w.w = pack_bf16x2(c.z * m, c.w * m);
+    w.x = pack2<F16>(a.x * m, a.y * m);
+    w.y = pack2<F16>(a.z * m, a.w * m);
+    w.z = pack2<F16>(c.x * m, c.y * m);
+    w.w = pack2<F16>(c.z * m, c.w * m);
     reinterpret_cast<uint4*>((which ? dk : dv) + (size_t)r * D)[g] = w;
   }
 }

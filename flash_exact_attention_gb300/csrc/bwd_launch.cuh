@@ -4,7 +4,7 @@
 
 namespace attn {
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, const void* o,
                             const void* dout, const float* lse, void* dq, cudaStream_t stream) {
@@ -19,13 +19,13 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     return cudaErrorInvalidValue;
   const long long prow = (long long)p.B * p.Hq * p.Npad;  // padded rows
   const long long kv_rows = split ? (long long)p.B * p.Hkv * p.Npad : 0;
-  bwd_preprocess<D><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse,
+  bwd_preprocess<D, F16><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
       const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dq_acc, prow, p.N, p.Npad,
       p.dk_acc, p.dv_acc, kv_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = bwd_kernel<D, CAUSAL>;
+  auto kern = bwd_kernel<D, CAUSAL, F16>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv) * (unsigned)p.gsplit;
@@ -34,15 +34,15 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
   if (e != cudaSuccess) return e;
   const long long orow = (long long)p.B * p.Hq * p.N;
   const long long groups = orow * (D / 8);
-  bwd_postprocess<D><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, static_cast<__nv_bfloat16*>(dq), orow, p.N, p.Npad, p.scale);
+  bwd_postprocess<D, F16><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
+      p.dq_acc, static_cast<uint16_t*>(dq), orow, p.N, p.Npad, p.scale);
   if (split) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long kvrow = (long long)p.B * p.Hkv * p.N;
     const long long kvgroups = kvrow * (D / 8);
-    bwd_post_kv<D><<<(unsigned)((kvgroups + 255) / 256), 256, 0, stream>>>(
-        p.dk_acc, p.dv_acc, static_cast<__nv_bfloat16*>(p.dk), static_cast<__nv_bfloat16*>(p.dv),
+    bwd_post_kv<D, F16><<<(unsigned)((kvgroups + 255) / 256), 256, 0, stream>>>(
+        p.dk_acc, p.dv_acc, static_cast<uint16_t*>(p.dk), static_cast<uint16_t*>(p.dv),
         kvrow, p.N, p.Npad, p.scale);
   }
   return cudaGetLastError();

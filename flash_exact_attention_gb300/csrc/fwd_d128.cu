@@ -1,10 +1,10 @@
-// Forward kernels for head dim 128 (causal and non-causal).
+// Forward kernels for head dim 128, bf16 inputs and output (causal and non-causal).
 #include "fwd_launch.cuh"
 
 namespace attn {
 cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdParams& p, bool causal, cudaStream_t stream) {
-  return causal ? launch_fwd_impl<128, true>(tq, tk, tv, p, stream)
-                : launch_fwd_impl<128, false>(tq, tk, tv, p, stream);
+                          const FwdParams& p, bool causal, cudaStream_t stream) {
+  return causal ? launch_fwd_impl<128, true, false>(tq, tk, tv, p, stream)
+                : launch_fwd_impl<128, false, false>(tq, tk, tv, p, stream);
 }
 }  // namespace attn

@@ -1,10 +1,10 @@
-// Forward kernels for head dim 64 (causal and non-causal).
+// Forward kernels for head dim 64, bf16 inputs and output (causal and non-causal).
 #include "fwd_launch.cuh"
 
 namespace attn {
 cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const FwdParams& p, bool causal, cudaStream_t stream) {
-  return causal ? launch_fwd_impl<64, true>(tq, tk, tv, p, stream)
-                : launch_fwd_impl<64, false>(tq, tk, tv, p, stream);
+                          const FwdParams& p, bool causal, cudaStream_t stream) {
+  return causal ? launch_fwd_impl<64, true, false>(tq, tk, tv, p, stream)
+                : launch_fwd_impl<64, false, false>(tq, tk, tv, p, stream);
 }
 }  // namespace attn

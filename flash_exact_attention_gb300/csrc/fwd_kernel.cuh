@@ -70,7 +70,7 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ MMA issuer
     regs_decrease<Cfg::kRegOther>();
     if (lane == 0) {
-      constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0);
-      constexpr uint32_t kIdescO = make_idesc_bf16(128, D, 1);
+      constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0, 0, F16);
+      constexpr uint32_t kIdescO = make_idesc_bf16(128, D, 1, 0, F16);
       const uint32_t q_addr[2] = {sbase + Cfg::kQOff, sbase + Cfg::kQOff + Cfg::kTileBytes};
       const uint32_t tS[2] = {tmem_base, tmem_base + 128};
       const uint32_t tO[2] = {tmem_base + 256, tmem_base + 384};
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(384, 1)
         const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, nm2);
         const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pp);
-        pk[c / 2] = pack_bf16x2(pp.x, pp.y);
+        pk[c / 2] = pack2<F16>(pp.x, pp.y);
         if (c == 62) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       }
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool live = grow < p.N;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
                                              ((size_t)bh * p.N + (size_t)(live ? grow : 0)) * D);
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
@@ -366,10 +366,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+            w.x = pack2<F16>(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+            w.y = pack2<F16>(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+            w.z = pack2<F16>(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+            w.w = pack2<F16>(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
             orow[c / 8 + v] = w;
           }
         }

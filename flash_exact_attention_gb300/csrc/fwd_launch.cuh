@@ -1,14 +1,14 @@
-// fwd_launch.cuh -- host-side launch of fwd_kernel<D, CAUSAL> (one grid per call).
+// fwd_launch.cuh -- host-side launch of fwd_kernel<D, CAUSAL, F16> (one grid per call).
 #pragma once
 #include "fwd_kernel.cuh"
 
 namespace attn {
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, CAUSAL, F16>;
   // Attributes are per device; setting them on every call is cheap and keeps
   // multi-device processes correct.
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -72,12 +72,14 @@ BwdScratch carve_scratch_split(void* base, int B, int Hq, int Hkv, int N, int D,
 int bwd_prepare(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 int B, int Hq, int Hkv, int N, int D, float scale, const void* dout, void* dq,
                 void* dk, void* dv, BwdParams* p, CUtensorMap* tq, CUtensorMap* tk,
-                CUtensorMap* tv, CUtensorMap* tdo, bool allow_split = false);
+                CUtensorMap* tv, CUtensorMap* tdo, bool allow_split = false,
+                bool f16 = false);
 
 // Enqueues the three backward kernels with the scratch already in `p`.
 int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
-               const float* lse, void* dq, int D, int causal, cudaStream_t s);
+               const float* lse, void* dq, int D, int causal, cudaStream_t s,
+               bool f16 = false);
 
 // Enqueues preprocess, main and postprocess kernels of the backward.
 cudaError_t launch_bwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -88,12 +90,21 @@ cudaError_t launch_bwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const BwdParams& p, const void* o,
                             const void* dout, const float* lse, void* dq, bool causal,
                             cudaStream_t stream);
+// The same for fp16 inputs and gradients.
+cudaError_t launch_bwd_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const BwdParams& p, const void* o,
+                               const void* dout, const float* lse, void* dq, bool causal,
+                               cudaStream_t stream);
+cudaError_t launch_bwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                                const void* o, const void* dout, const float* lse, void* dq,
+                                bool causal, cudaStream_t stream);
 
 // Host helpers shared by the entry points (attn_api.cu).
 int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale);
 int device_setup(int* dev_out, unsigned int** err_out);
 int device_sm_count(int dev);
-int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH);
+int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16 = false);
 int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH);
 uint64_t wait_timeout_ns();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -103,10 +114,17 @@ cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const C
                            const FwdParams& p, bool causal, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, bool causal, cudaStream_t stream);
+cudaError_t launch_fwd_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const FwdParams& p, bool causal, cudaStream_t stream);
+cudaError_t launch_fwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const FwdParams& p, bool causal,
+                                cudaStream_t stream);
 
 // Entry points behind the C ABI (attn_api.cu, bwd.cu).
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
               int Hq, int Hkv, int N, int D, int causal, float scale, void* stream,
-              const void* dout, void* dq, void* dk, void* dv);
+              const void* dout, void* dq, void* dk, void* dv, bool f16 = false);
+int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+              int Hkv, int N, int D, int causal, float scale, void* stream, bool f16 = false);
 
 }  // namespace attn

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace attn {
 
@@ -277,10 +278,10 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M x N
 // tile; a_mn / b_mn select an MN-major (1) instead of K-major (0) operand.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t M, uint32_t N, uint32_t b_mn_major,
-                                                       uint32_t a_mn_major = 0) {
+                                                       uint32_t a_mn_major = 0, bool f16 = false) {
   return (1u << 4)                 // D format: f32
-         | (1u << 7)               // A format: bf16
-         | (1u << 10)              // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)  // A format: bf16 (1) or f16 (0)
+         | ((f16 ? 0u : 1u) << 10) // B format: bf16 (1) or f16 (0)
          | (a_mn_major << 15)      // A major-ness
          | (b_mn_major << 16)      // B major-ness
          | ((N >> 3) << 17)        // N / 8
@@ -460,6 +461,28 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// The kernels' 16-bit element type: bf16 (F16 = false) or IEEE fp16 (F16 = true).
+// pack2 rounds two fp32 values to nearest-even and packs them (lo in the low half).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
+}
+
+// Exact widening of a packed pair to fp32 (x = low half).
+template <bool F16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  if constexpr (F16) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&u));
+  } else {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  }
 }
 
 }  // namespace attn

@@ -1,7 +1,7 @@
 """Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
 
 This module holds no attention arithmetic: it only draws iid N(0,1) numbers and
-rounds them to bf16.  Recipe: ``numpy.random.default_rng(seed)`` draws fp32
+rounds them to bf16 (or, for the fp16 entry points, to fp16).  Recipe: ``numpy.random.default_rng(seed)`` draws fp32
 ``standard_normal`` arrays in the order Q, K, V, dO; each is rounded to bf16
 with round-to-nearest-even on the bit pattern.  The same bit patterns feed the
 CUDA path (as bf16 tensors) and the fp64 oracle (widened exactly).
@@ -27,6 +27,16 @@ def make_inputs(B, Hq, Hkv, N, D, seed, with_do=False):
     out = {}
     for name, h in (("q", Hq), ("k", Hkv), ("v", Hkv)) + ((("do", Hq),) if with_do else ()):
         out[name] = f32_to_bf16_bits(rng.standard_normal((B, h, N, D), dtype=np.float32))
+    return out
+
+
+def make_inputs_f16(B, Hq, Hkv, N, D, seed, with_do=False):
+    """The same draws as make_inputs, rounded to IEEE fp16 instead (numpy's
+    float32 -> float16 conversion rounds to nearest even); fp16 arrays."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for name, h in (("q", Hq), ("k", Hkv), ("v", Hkv)) + ((("do", Hq),) if with_do else ()):
+        out[name] = rng.standard_normal((B, h, N, D), dtype=np.float32).astype(np.float16)
     return out
 
 

@@ -89,6 +89,23 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o,
              void* dv);
 
 /*
+ * The same two calls for IEEE fp16 (binary16) q, k, v, o, dout, dq, dk, dv
+ * instead of bf16 (FlashAttention for Tesla P100, "What it supports": fp16
+ * inputs with fp32 accumulation).  Arguments, layouts, scratch, results and
+ * error codes are those of attn_fwd / attn_bwd; lse stays fp32.  P and dS are
+ * rounded to fp16 for the tensor cores (P <= 2^8 and |dS| well inside fp16's
+ * range for attention inputs); every accumulation is fp32.  Results that
+ * exceed fp16's range (|x| > 65504) become +-inf.
+ */
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int N, int D, int causal, float scale,
+                 void* stream);
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                 float scale, void* stream, const void* dout, void* dq, void* dk,
+                 void* dv);
+
+/*
  * Backward without any device allocation.  No counterpart in the paper: this
  * is a deployment variant of attn_bwd for callers that cannot call the CUDA
  * allocator -- a process whose device memory is owned by its own pool, or a
