@@ -29,6 +29,8 @@ SIGNATURES = {
     "attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P],
                          _I),
     "attn_fwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_bwd_deterministic": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
+                                _P], _I),
     "attn_bwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
     "attn_bwd_noalloc_scratch_limit": ([], ctypes.c_longlong),
     "attn_status_string": ([_I], ctypes.c_char_p),
@@ -111,6 +113,15 @@ def attn_bwd_f16(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout,
                                _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
 
 
+def attn_bwd_deterministic(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq,
+                           dk, dv):
+    """Raw call of the run-to-run bitwise-reproducible backward (bf16)."""
+    return load().attn_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
+                                         Hkv, N, D, int(bool(causal)), float(scale),
+                                         _stream_handle(stream), _ptr(dout), _ptr(dq), _ptr(dk),
+                                         _ptr(dv))
+
+
 def attn_bwd_noalloc(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
                      dv):
     """Raw call of the backward that allocates nothing (fixed scratch array)."""
@@ -167,8 +178,10 @@ def flash_attn(q, k, v, causal=False, scale=None, stream=None):
     return o, lse
 
 
-def flash_attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, stream=None):
-    """dQ, dK, dV of sum(dout * O) given the forward's O and LSE."""
+def flash_attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, stream=None,
+                   deterministic=False):
+    """dQ, dK, dV of sum(dout * O) given the forward's O and LSE.  With
+    deterministic=True (bf16 only) the results are bitwise reproducible."""
     import torch
     B, Hq, N, D = q.shape
     Hkv = k.shape[1]
@@ -181,7 +194,12 @@ def flash_attn_bwd(q, k, v, o, lse, dout, causal=False, scale=None, stream=None)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    call = attn_bwd_f16 if q.dtype == torch.float16 else attn_bwd
+    if deterministic:
+        if q.dtype != torch.bfloat16:
+            raise ValueError("the deterministic backward takes bf16 tensors")
+        call = attn_bwd_deterministic
+    else:
+        call = attn_bwd_f16 if q.dtype == torch.float16 else attn_bwd
     st = call(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk, dv)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")

@@ -223,6 +223,14 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                          dv, true);
 }
 
+int attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                           float scale, void* stream, const void* dout, void* dq, void* dk,
+                           void* dv) {
+  return attn::bwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
+                         dv, false, true);
+}
+
 const char* attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ok";

@@ -97,9 +97,12 @@ int bwd_prepare(const void* q, const void* k, const void* v, const void* o,
 
 int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
-                      const float* lse, void* dq, int D, int causal, cudaStream_t s, bool f16) {
+                      const float* lse, void* dq, int D, int causal, cudaStream_t s, bool f16,
+                      bool det) {
   const bool c = causal != 0;
   cudaError_t e =
+      det ? ((D == 64) ? launch_bwd_det_d64(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s)
+                       : launch_bwd_det_d128(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s)) :
       f16 ? ((D == 64) ? launch_bwd_d64_f16(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s)
                        : launch_bwd_d128_f16(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s))
           : ((D == 64) ? launch_bwd_d64(tq, tk, tv, tdo, p, o, dout, lse, dq, c, s)
@@ -109,24 +112,31 @@ int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
 
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
               int Hq, int Hkv, int N, int D, int causal, float scale, void* stream,
-              const void* dout, void* dq, void* dk, void* dv, bool f16) {
+              const void* dout, void* dq, void* dk, void* dv, bool f16, bool det) {
   BwdParams p;
   CUtensorMap tq, tk, tv, tdo;
   int st = bwd_prepare(q, k, v, o, lse, B, Hq, Hkv, N, D, scale, dout, dq, dk, dv, &p, &tq, &tk,
-                       &tv, &tdo, /*allow_split=*/true, f16);
+                       &tv, &tdo, /*allow_split=*/!det, f16);
   if (st == -1) return ATTN_OK;
   if (st != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, bwd_scratch_bytes_split(B, Hq, Hkv, N, D, p.gsplit), s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  const BwdScratch sc = carve_scratch_split(ws, B, Hq, Hkv, N, D, p.gsplit);
+  // The deterministic backward needs only LSE2 and Delta (no dQ accumulator).
+  const size_t rows = (size_t)B * Hq * (size_t)p.Npad;
+  const size_t bytes = det ? 2 * rows * 4 : bwd_scratch_bytes_split(B, Hq, Hkv, N, D, p.gsplit);
+  if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  BwdScratch sc = carve_scratch_split(ws, B, Hq, Hkv, N, D, p.gsplit);
+  if (det) {
+    sc.dq_acc = nullptr;
+    sc.lse2 = static_cast<float*>(ws);
+    sc.delta = sc.lse2 + rows;
+  }
   p.dq_acc = sc.dq_acc;
   p.lse2 = sc.lse2;
   p.delta = sc.delta;
   p.dk_acc = sc.dk_acc;
   p.dv_acc = sc.dv_acc;
-  st = bwd_launch(tq, tk, tv, tdo, p, o, dout, lse, dq, D, causal, s, f16);
+  st = bwd_launch(tq, tk, tv, tdo, p, o, dout, lse, dq, D, causal, s, f16, det);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == ATTN_OK) st = ATTN_ERR_CUDA;
   return st;
 }

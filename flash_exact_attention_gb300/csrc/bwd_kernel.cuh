@@ -94,7 +94,8 @@ struct BwdCfg {
   static_assert(kTile + 2 * kBox >= (D / 32) * kBox, "dK partial staging");
 };
 
-template <int D, bool CAUSAL, bool F16>
+// DQ = false: dK and dV only (the deterministic backward computes dQ in bwd_dq_kernel).
+template <int D, bool CAUSAL, bool F16, bool DQ = true>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_dq);
+    if (DQ) tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -279,7 +280,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t mQs_ = mQ0 + s * kQs, kQn = kQ0 + (s ^ 1) * kQs;
         // dP_it over the dP^T columns, once dQ_{it-1} has been read out of them.
         if (!mbar_wait_tested_inl(bar_do_full, (uint32_t)it & 1u, wc)) return false;
-        if (!kOwnDq && it > 0 && !mbar_wait_tested_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
+        if (DQ && !kOwnDq && it > 0 &&
+            !mbar_wait_tested_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
           return false;
         tc_fence_after();
         issue_t(tdP, kV, kdO);
@@ -307,12 +309,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss_w(tdK, kdS, koff(kk), mQs_, moff(kk), kHi, kIdescB_MN,
                    (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar_q_free(s));
-        if (kOwnDq && it > 0 && !mbar_wait_tested_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
-          return false;
+        if (DQ) {
+          if (kOwnDq && it > 0 &&
+              !mbar_wait_tested_inl(bar_dq_free, (uint32_t)(it - 1) & 1u, wc))
+            return false;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys)
-          mma_ss_w(tdQ, mdS, moff(kk), mK, moff(kk), kHi, kIdescDQ, kk > 0);
-        mma_commit(bar_dq);
+          for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K = 128 keys)
+            mma_ss_w(tdQ, mdS, moff(kk), mK, moff(kk), kHi, kIdescDQ, kk > 0);
+          mma_commit(bar_dq);
+        }
         return true;
       };
       bool ok = mbar_wait_tested_inl(bar_kv, 0, wc) && mbar_wait_tested_inl(bar_q_full(0), 0, wc);
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t st_row = sbase + Cfg::kdQ + (uint32_t)qrow * 128u;
     int chunk = 0;
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0; it < (DQ ? n_it : 0); ++it) {
       // One decision for the whole warpgroup: its named barriers need all 4 warps.
       ok = named_bar_and(1, 128, mbar_wait_tested_inl(bar_dq, (uint32_t)it & 1u, wc));
       if (!ok) break;
@@ -592,9 +597,11 @@ __global__ void __launch_bounds__(256)
     lse2[r] = i < N ? lse[(size_t)bh * N + i] * 1.4426950408889634f : INFINITY;
     delta[r] = acc;
   }
-  float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)r * D);
+  if (dq_acc != nullptr) {  // none in the deterministic backward
+    float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)r * D);
 #pragma unroll
-  for (int t = lane; t < D / 4; t += 32) z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = lane; t < D / 4; t += 32) z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (r < kv_rows) {  // group split: zero the dK/dV accumulators too
     float4* zk = reinterpret_cast<float4*>(dk_acc + (size_t)r * D);
     float4* zv = reinterpret_cast<float4*>(dv_acc + (size_t)r * D);

@@ -1,16 +1,21 @@
 // bwd_launch.cuh -- host-side launch of the three backward kernels for one head dim.
 #pragma once
 #include "bwd_kernel.cuh"
+#include "bwd_dq_kernel.cuh"
 
 namespace attn {
 
-template <int D, bool CAUSAL, bool F16>
+// DQ = false: the deterministic backward (dK/dV kernel, then bwd_dq_kernel).
+template <int D, bool CAUSAL, bool F16, bool DQ = true>
 cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdParams& p, const void* o,
                             const void* dout, const float* lse, void* dq, cudaStream_t stream) {
   using Cfg = BwdCfg<D>;
-  CUtensorMap tdq;  // the fp32 dQ accumulator, target of the TMA reduce-add
-  if (encode_f32_rows_map(&tdq, p.dq_acc, D, p.Npad, p.B * p.Hq) != 0) return cudaErrorInvalidValue;
+  // The fp32 dQ accumulator, target of the TMA reduce-add (none without DQ: the
+  // kernel then never touches the map, which is left a copy of a valid one).
+  CUtensorMap tdq = tq;
+  if (DQ && encode_f32_rows_map(&tdq, p.dq_acc, D, p.Npad, p.B * p.Hq) != 0)
+    return cudaErrorInvalidValue;
   // Group split: the fp32 dK/dV accumulators (else unused: any valid map).
   CUtensorMap tdk = tdq, tdv = tdq;
   const bool split = p.gsplit > 1;
@@ -25,7 +30,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
       p.dk_acc, p.dv_acc, kv_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = bwd_kernel<D, CAUSAL, F16>;
+  auto kern = bwd_kernel<D, CAUSAL, F16, DQ>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv) * (unsigned)p.gsplit;
@@ -33,9 +38,19 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long orow = (long long)p.B * p.Hq * p.N;
-  const long long groups = orow * (D / 8);
-  bwd_postprocess<D, F16><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, static_cast<uint16_t*>(dq), orow, p.N, p.Npad, p.scale);
+  if (DQ) {
+    const long long groups = orow * (D / 8);
+    bwd_postprocess<D, F16><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
+        p.dq_acc, static_cast<uint16_t*>(dq), orow, p.N, p.Npad, p.scale);
+  } else {
+    using DCfg = DqCfg<D>;
+    auto dkern = bwd_dq_kernel<D, CAUSAL, F16>;
+    e = cudaFuncSetAttribute(dkern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned dgrid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hq);
+    dkern<<<dgrid, DCfg::kThreads, DCfg::kSmemBytes, stream>>>(tq, tk, tv, tdo, p,
+                                                               static_cast<uint16_t*>(dq));
+  }
   if (split) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

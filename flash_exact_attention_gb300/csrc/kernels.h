@@ -79,7 +79,7 @@ int bwd_prepare(const void* q, const void* k, const void* v, const void* o, cons
 int bwd_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
                const float* lse, void* dq, int D, int causal, cudaStream_t s,
-               bool f16 = false);
+               bool f16 = false, bool det = false);
 
 // Enqueues preprocess, main and postprocess kernels of the backward.
 cudaError_t launch_bwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -90,6 +90,15 @@ cudaError_t launch_bwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const CUtensorMap& tdo, const BwdParams& p, const void* o,
                             const void* dout, const float* lse, void* dq, bool causal,
                             cudaStream_t stream);
+// The deterministic backward (bf16): dK/dV kernel without dQ, then dQ per query tile.
+cudaError_t launch_bwd_det_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const BwdParams& p, const void* o,
+                               const void* dout, const float* lse, void* dq, bool causal,
+                               cudaStream_t stream);
+cudaError_t launch_bwd_det_d128(const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                                const void* o, const void* dout, const float* lse, void* dq,
+                                bool causal, cudaStream_t stream);
 // The same for fp16 inputs and gradients.
 cudaError_t launch_bwd_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tdo, const BwdParams& p, const void* o,
@@ -123,7 +132,8 @@ cudaError_t launch_fwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
 // Entry points behind the C ABI (attn_api.cu, bwd.cu).
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
               int Hq, int Hkv, int N, int D, int causal, float scale, void* stream,
-              const void* dout, void* dq, void* dk, void* dv, bool f16 = false);
+              const void* dout, void* dq, void* dk, void* dv, bool f16 = false,
+              bool det = false);
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
               int Hkv, int N, int D, int causal, float scale, void* stream, bool f16 = false);
 

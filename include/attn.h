@@ -106,6 +106,22 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o,
                  void* dv);
 
 /*
+ * Deterministic backward (bf16): the arguments, layouts and error codes of
+ * attn_bwd, with results that are bitwise identical from run to run.
+ * attn_bwd adds each key tile's fp32 dQ partial into an accumulator in
+ * arrival order, so dQ's last bits vary between runs; here dK and dV come from
+ * the same kernel without those adds, and dQ from a second kernel that owns a
+ * query tile and sums its key tiles in a fixed order (recomputing S and dP:
+ * 7 MMAs per (query, key) tile pair instead of 5).  A GQA group is never split
+ * across CTAs on this path.  Scratch: fp32 LSE2 and Delta only
+ * (cudaMallocAsync/cudaFreeAsync on `stream`).
+ */
+int attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,
+                           float scale, void* stream, const void* dout, void* dq, void* dk,
+                           void* dv);
+
+/*
  * Backward without any device allocation.  No counterpart in the paper: this
  * is a deployment variant of attn_bwd for callers that cannot call the CUDA
  * allocator -- a process whose device memory is owned by its own pool, or a
