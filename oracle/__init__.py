@@ -4,7 +4,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg (and its ``--impl reference`` arm) may import this package.  The CUDA
 library never calls it and shares no code with it.
 
-``attn_oracle.c`` holds the arithmetic (plain definition, fp64, OpenMP);
+``attn_oracle.c`` holds the arithmetic (plain definition, fp64, OpenMP) of
+softmax attention and of Stieltjes attention;
 this module compiles it with gcc and calls it through ctypes.  Inputs may be
 any array-likes of bf16-representable values: they are widened to fp64
 exactly before the call.  Every function here follows the definitions cited
@@ -47,6 +48,9 @@ def bind(lib):
     lib.oracle_fwd_rows.restype = i
     lib.oracle_bwd.argtypes = [d, d, d, d, i, i, i, i, i, i, ctypes.c_double, d, d, d]
     lib.oracle_bwd.restype = i
+    lib.oracle_stj_fwd_rows.argtypes = [d, d, d, i, i, i, i, i, i, ctypes.c_double, i, i,
+                                        ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, d, d]
+    lib.oracle_stj_fwd_rows.restype = i
     lib.oracle_num_threads.restype = i
     return lib
 
@@ -121,3 +125,35 @@ def bwd(q, k, v, do, causal, scale):
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     return dq, dk, dv
+
+
+def stj_fwd_rows(q, k, v, causal, scale, order, steps, rows=None):
+    """Stieltjes attention for selected rows: (o [len(rows), D], pole [len(rows)]).
+
+    The pole is returned in score units (row max + Newton's lambda); steps <= 0
+    solves for the exact pole instead of running `steps` Newton steps."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    if rows is None:
+        nrows = B * Hq * N
+        rptr = None
+    else:
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows.size
+        rptr = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    o = np.empty((nrows, D), dtype=np.float64)
+    pole = np.empty((nrows,), dtype=np.float64)
+    rc = _load().oracle_stj_fwd_rows(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N, D,
+                                     int(bool(causal)), float(scale), int(order), int(steps),
+                                     rptr, nrows, _ptr(o), _ptr(pole))
+    if rc != 0:
+        raise ValueError("oracle_stj_fwd_rows rejected its arguments")
+    return o, pole
+
+
+def stj_fwd(q, k, v, causal, scale, order, steps):
+    """Full Stieltjes forward: (o [B,Hq,N,D], pole [B,Hq,N]) in fp64."""
+    B, Hq, N, D = tuple(q.shape)
+    o, pole = stj_fwd_rows(q, k, v, causal, scale, order, steps)
+    return o.reshape(B, Hq, N, D), pole.reshape(B, Hq, N)

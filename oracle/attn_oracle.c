@@ -211,3 +211,86 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
   }
   return err;
 }
+
+/*
+ * Stieltjes attention forward, a second method on the same tiling (SURVEY's
+ * next-ranked row).  FlashStieltjes page, "Why touch softmax": weights
+ * p_j = (lambda - s_j)^-q with the pole lambda above the best score, placed so
+ * that the weights add up to 1; "The challenge": subtract the row's largest
+ * score, then Newton-Raphson from lambda = 1.1 (three steps by default);
+ * "The kernel": sweep 1 the row max, sweeps 2-4 the Newton steps, sweep 5
+ * weights and values.  For each row, over its allowed keys:
+ *
+ *   m   = max_j s_j,   t_j = s_j - m  (<= 0)
+ *   f(l) = sum_j (l - t_j)^-q - 1,   f'(l) = -q sum_j (l - t_j)^-(q+1)
+ *   l_0 = 1.1,  l_{n+1} = l_n - f(l_n) / f'(l_n)   (`steps` times)
+ *   p_j = (l - t_j)^-q,   O = sum_j p_j v_j,   pole = m + l
+ *
+ * steps <= 0 iterates to convergence instead (step below 1e-15 l, at most 200
+ * steps): the exact pole, for the tests' closed forms.  The weights are used
+ * as they come out of the last step (no renormalisation), as the page's fifth
+ * sweep does.
+ */
+static double row_stj_pole(const double* s, int64_t n, int order, int steps) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) if (s[j] > m) m = s[j];
+  double l = 1.1;
+  const int limit = steps > 0 ? steps : 200;
+  for (int it = 0; it < limit; ++it) {
+    double f = -1.0, fp = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      const double a = l - (s[j] - m);
+      f += pow(a, -(double)order);
+      fp += -(double)order * pow(a, -(double)(order + 1));
+    }
+    const double step = f / fp;
+    l -= step;
+    if (steps <= 0 && fabs(step) <= 1e-15 * l) break;
+  }
+  return m + l;
+}
+
+int oracle_stj_fwd_rows(const double* q, const double* k, const double* v,
+                        int B, int Hq, int Hkv, int N, int D, int causal, double scale,
+                        int order, int steps, const int64_t* rows, int64_t nrows,
+                        double* o, double* pole) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || D <= 0 || Hq % Hkv || order < 1) return -1;
+  const int64_t G = Hq / Hkv;
+  const int64_t total = (int64_t)B * Hq * N;
+  if (!rows) nrows = total;
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+    if (!s) {
+#pragma omp atomic write
+      err = -1;
+    }
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t r = 0; r < nrows; ++r) {
+      if (!s) continue;
+      int64_t id = rows ? rows[r] : r;
+      if (id < 0 || id >= total) {
+#pragma omp atomic write
+        err = -1;
+        continue;
+      }
+      int64_t i = id % N, bh = id / N, h = bh % Hq, b = bh / Hq, hk = h / G;
+      const double* qi = q + at4(b, h, i, 0, Hq, N, D);
+      const double* kh = k + at4(b, hk, 0, 0, Hkv, N, D);
+      const double* vh = v + at4(b, hk, 0, 0, Hkv, N, D);
+      int64_t n = row_scores(qi, kh, N, D, i, causal, scale, s);
+      const double pl = row_stj_pole(s, n, order, steps);
+      pole[r] = pl;
+      double* oi = o + r * (int64_t)D;
+      for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+      for (int64_t j = 0; j < n; ++j) {
+        const double pj = pow(pl - s[j], -(double)order);
+        const double* vj = vh + j * D;
+        for (int64_t d = 0; d < D; ++d) oi[d] += pj * vj[d];
+      }
+    }
+    free(s);
+  }
+  return err;
+}

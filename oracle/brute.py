@@ -93,3 +93,35 @@ def brute_bwd(q, k, v, do, B, Hq, Hkv, N, D, causal, scale):
     dk = [math.fsum(t) for t in dk_terms]
     dv = [math.fsum(t) for t in dv_terms]
     return dq, dk, dv
+
+
+def brute_stj_fwd(q, k, v, B, Hq, Hkv, N, D, causal, scale, order, steps):
+    """Stieltjes attention (FlashStieltjes page, "Why touch softmax" and "The
+    challenge"): per row, m = max score, Newton from 1.1 on
+    sum (l - (s - m))^-q = 1 for `steps` steps, weights (m + l - s)^-q.
+    Returns (o, pole) as flat lists; pole = m + l."""
+    G = Hq // Hkv
+    qs, ks = (B, Hq, N, D), (B, Hkv, N, D)
+    o = [0.0] * (B * Hq * N * D)
+    pole = [0.0] * (B * Hq * N)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            for i in range(N):
+                qi = _row(q, qs, b, h, i)
+                keys = range(i + 1) if causal else range(N)
+                s = [scale * math.fsum(a * c for a, c in zip(qi, _row(k, ks, b, hk, j)))
+                     for j in keys]
+                m = max(s)
+                lam = 1.1
+                for _ in range(steps):
+                    f = math.fsum((lam - (x - m)) ** (-order) for x in s) - 1.0
+                    fp = -order * math.fsum((lam - (x - m)) ** (-order - 1) for x in s)
+                    lam -= f / fp
+                pole[(b * Hq + h) * N + i] = m + lam
+                w = [(m + lam - x) ** (-order) for x in s]
+                base = _idx(qs, b, h, i)
+                for d in range(D):
+                    o[base + d] = math.fsum(w[t] * _row(v, ks, b, hk, j)[d]
+                                            for t, j in enumerate(keys))
+    return o, pole
