@@ -29,6 +29,7 @@ SIGNATURES = {
     "attn_bwd_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P],
                          _I),
     "attn_fwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_stieltjes_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_bwd_deterministic": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
                                 _P], _I),
     "attn_bwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
@@ -111,6 +112,14 @@ def attn_bwd_f16(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout,
     return load().attn_bwd_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, D,
                                int(bool(causal)), float(scale), _stream_handle(stream),
                                _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
+
+
+def attn_stieltjes_fwd(q, k, v, o, pole, B, Hq, Hkv, N, D, causal, scale, order, newton_steps,
+                       stream=None):
+    """Raw call of the Stieltjes attention forward; returns the status code."""
+    return load().attn_stieltjes_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(pole), B, Hq, Hkv,
+                                     N, D, int(bool(causal)), float(scale), int(order),
+                                     int(newton_steps), _stream_handle(stream))
 
 
 def attn_bwd_deterministic(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq,
@@ -243,3 +252,24 @@ def attention(q, k, v, causal=False, scale=None):
     o, _ = _attn_function().apply(q, k, v, bool(causal),
                                   1.0 / math.sqrt(q.shape[-1]) if scale is None else scale)
     return o
+
+
+def stieltjes_attn(q, k, v, causal=False, scale=None, order=4, newton_steps=3, stream=None):
+    """Stieltjes attention (FlashStieltjes page): O and the per-row pole for bf16
+    CUDA tensors q [B,Hq,N,D], k/v [B,Hkv,N,D]; order 2 or 4, newton_steps Newton
+    steps from 1.1 above the row max (the page's default is 3)."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    _check(q, (B, Hq, N, D), "q", torch.bfloat16)
+    _check(k, (B, Hkv, N, D), "k", torch.bfloat16)
+    _check(v, (B, Hkv, N, D), "v", torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    pole = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    st = attn_stieltjes_fwd(q, k, v, o, pole, B, Hq, Hkv, N, D, causal, scale, order,
+                            newton_steps, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_stieltjes_fwd")
+    return o, pole

@@ -173,6 +173,48 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int stj_entry(const void* q, const void* k, const void* v, void* o, float* pole, int B, int Hq,
+              int Hkv, int N, int D, int causal, float scale, int order, int steps,
+              void* stream) {
+  int st = validate_shape(B, Hq, Hkv, N, D, scale);
+  if (st != ATTN_OK) return st;
+  if (order != 2 && order != 4) return ATTN_ERR_UNSUPPORTED;
+  if (steps < 1 || steps > 64) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * Hq * N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !pole) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(pole))
+    return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  unsigned int* err = nullptr;
+  st = device_setup(&dev, &err);
+  if (st != ATTN_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (encode_tile_map(&tq, q, D, N, B * Hq) != ATTN_OK ||
+      encode_tile_map(&tk, k, D, N, B * Hkv) != ATTN_OK ||
+      encode_tile_map(&tv, v, D, N, B * Hkv) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  FwdParams p;
+  p.o = o;
+  p.lse = pole;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.G = Hq / Hkv;
+  p.num_qblocks = ((N + 127) / 128 + 1) / 2;
+  p.zigzag = 0;
+  p.num_kv_tiles = (N + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_timeout_ns();
+  p.err = err;
+  p.scale = scale;
+  p.steps = steps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (D == 64) ? launch_stj_d64(tq, tk, tv, p, causal != 0, order, s)
+                            : launch_stj_d128(tq, tk, tv, p, causal != 0, order, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int device_status(void* stream) {
   int dev = 0;
   unsigned int* err = nullptr;
@@ -221,6 +263,13 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  const void* dout, void* dq, void* dk, void* dv) {
   return attn::bwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
                          dv, true);
+}
+
+int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, float* pole, int B,
+                       int Hq, int Hkv, int N, int D, int causal, float scale, int order,
+                       int newton_steps, void* stream) {
+  return attn::stj_entry(q, k, v, o, pole, B, Hq, Hkv, N, D, causal, scale, order, newton_steps,
+                         stream);
 }
 
 int attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,

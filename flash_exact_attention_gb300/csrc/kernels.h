@@ -19,6 +19,10 @@ struct FwdParams {
   float scale_log2;     // scale * log2(e)
   uint64_t timeout_ns;  // limit of every device-side wait
   unsigned int* err;    // device error word
+  // Stieltjes forward only (lse then holds the pole): the softmax scale and
+  // the number of Newton steps.
+  float scale;
+  int steps;
 };
 
 // Backward parameters of the main kernel (everything but the tensor maps).
@@ -128,6 +132,12 @@ cudaError_t launch_fwd_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk, con
 cudaError_t launch_fwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const FwdParams& p, bool causal,
                                 cudaStream_t stream);
+
+// Stieltjes attention forward (order 2 or 4), one kernel per call.
+cudaError_t launch_stj_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const FwdParams& p, bool causal, int order, cudaStream_t stream);
+cudaError_t launch_stj_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, bool causal, int order, cudaStream_t stream);
 
 // Entry points behind the C ABI (attn_api.cu, bwd.cu).
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,

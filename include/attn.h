@@ -106,6 +106,22 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o,
                  void* dv);
 
 /*
+ * Stieltjes attention forward (bf16; FlashStieltjes page, "Why touch softmax",
+ * "The challenge", "The kernel"): weights p_j = (lambda - s_j)^-order over the
+ * allowed keys, s = scale * q.k, with the pole lambda found per row by
+ * newton_steps Newton-Raphson steps on sum_j (lambda - s_j)^-order = 1 from
+ * 1.1 above the row maximum (the page's kernel runs 3); o = sum_j p_j v_j
+ * (bf16 [B,Hq,N,D]), pole = lambda in score units (fp32 [B,Hq,N]).  The keys
+ * are streamed newton_steps + 2 times.  Other arguments, layouts and errors as
+ * attn_fwd; order must be 2 or 4 (else ATTN_ERR_UNSUPPORTED), 1 <= newton_steps
+ * <= 64 (else ATTN_ERR_INVALID_ARG).  Weights are used as the last step leaves
+ * them: rows whose Newton iteration has not converged are not renormalised.
+ */
+int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, float* pole,
+                       int B, int Hq, int Hkv, int N, int D, int causal, float scale, int order,
+                       int newton_steps, void* stream);
+
+/*
  * Deterministic backward (bf16): the arguments, layouts and error codes of
  * attn_bwd, with results that are bitwise identical from run to run.
  * attn_bwd adds each key tile's fp32 dQ partial into an accumulator in
