@@ -5,7 +5,7 @@ leg (and its ``--impl reference`` arm) may import this package.  The CUDA
 library never calls it and shares no code with it.
 
 ``attn_oracle.c`` holds the arithmetic (plain definition, fp64, OpenMP) of
-softmax attention and of Stieltjes attention;
+softmax attention, of Stieltjes attention and of Nystrom attention;
 this module compiles it with gcc and calls it through ctypes.  Inputs may be
 any array-likes of bf16-representable values: they are widened to fp64
 exactly before the call.  Every function here follows the definitions cited
@@ -51,6 +51,11 @@ def bind(lib):
     lib.oracle_stj_fwd_rows.argtypes = [d, d, d, i, i, i, i, i, i, ctypes.c_double, i, i,
                                         ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, d, d]
     lib.oracle_stj_fwd_rows.restype = i
+    lib.oracle_ns_pinv.argtypes = [d, i, i, ctypes.c_double, d]
+    lib.oracle_ns_pinv.restype = i
+    lib.oracle_nys_fwd.argtypes = [d, d, d, i, i, i, i, i, i, i, ctypes.c_double,
+                                   ctypes.c_double, d, d, d, d, d]
+    lib.oracle_nys_fwd.restype = i
     lib.oracle_num_threads.restype = i
     return lib
 
@@ -157,3 +162,41 @@ def stj_fwd(q, k, v, causal, scale, order, steps):
     B, Hq, N, D = tuple(q.shape)
     o, pole = stj_fwd_rows(q, k, v, causal, scale, order, steps)
     return o.reshape(B, Hq, N, D), pole.reshape(B, Hq, N)
+
+
+def ns_pinv(a, iters, kappa):
+    """Newton-Schulz pseudo-inverse of a square matrix after `iters` steps
+    (Tikhonov ridge when kappa > 0), as the Nystrom forward takes it."""
+    a = _f64(a)
+    m = a.shape[0]
+    if a.shape != (m, m):
+        raise ValueError("ns_pinv wants a square matrix")
+    out = np.empty((m, m), dtype=np.float64)
+    if _load().oracle_ns_pinv(_ptr(a), m, int(iters), float(kappa), _ptr(out)) != 0:
+        raise ValueError("oracle_ns_pinv rejected its arguments")
+    return out
+
+
+def nys_fwd(q, k, v, m, iters, kappa, scale, intermediates=False):
+    """Nystrom attention forward: o [B,Hq,N,D] in fp64.
+
+    With intermediates=True returns (o, dict(qt, kt, pinv, w)): the landmarks
+    Qt [B,Hq,m,D] and Kt [B,Hkv,m,D], the pseudo-inverse of the landmark
+    softmax [B,Hq,m,m] and W = softmax(scale Qt K^T) V [B,Hq,m,D]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    o = np.empty_like(q)
+    qt = np.empty((B, Hq, m, D)) if intermediates else None
+    kt = np.empty((B, Hkv, m, D)) if intermediates else None
+    pinv = np.empty((B, Hq, m, m)) if intermediates else None
+    w = np.empty((B, Hq, m, D)) if intermediates else None
+    opt = lambda a: _ptr(a) if a is not None else None
+    rc = _load().oracle_nys_fwd(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N, D, int(m),
+                                int(iters), float(kappa), float(scale), _ptr(o),
+                                opt(qt), opt(kt), opt(pinv), opt(w))
+    if rc != 0:
+        raise ValueError("oracle_nys_fwd rejected its arguments")
+    if intermediates:
+        return o, dict(qt=qt, kt=kt, pinv=pinv, w=w)
+    return o

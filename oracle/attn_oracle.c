@@ -294,3 +294,230 @@ int oracle_stj_fwd_rows(const double* q, const double* k, const double* v,
   }
   return err;
 }
+
+/*
+ * Nystrom attention forward (SURVEY's third next-ranked row).  FlashNystrom
+ * page, "Scope": the factorisation
+ *
+ *   O = softmax(Q Kt^T) . pinv(softmax(Qt Kt^T)) . softmax(Qt K^T) . V
+ *
+ * with landmarks Qt, Kt the segment means of Q and K, and the pseudo-inverse
+ * taken by a fixed number of unrolled Newton-Schulz steps; "Configuration":
+ * with the Tikhonov ridge on (kappa* > 0) the iteration inverts
+ * M = A^T A + lambda I, lambda = ||A||_1 ||A||_inf / kappa*, for A the m x m
+ * landmark softmax.  Readings taken where the page is silent:
+ *   - landmark i averages rows floor(i N / m) .. floor((i+1) N / m) - 1
+ *     (every segment non-empty since N >= m);
+ *   - the caller's scale multiplies all three score matrices;
+ *   - Newton-Schulz is the textbook pseudo-inverse iteration
+ *     X_0 = A^T / (||A||_1 ||A||_inf),  X_{t+1} = 2 X_t - X_t A X_t;
+ *   - with the ridge, pinv(A) is taken as X(M) A^T, X(M) the iteration on M;
+ *   - a query head h uses key/value head h / (Hq / Hkv), whose landmarks Kt
+ *     come from that key head's rows.
+ */
+
+/* max column sum (1-norm) and max row sum (inf-norm) of an m x m matrix */
+static double mat_norm1(const double* a, int m) {
+  double best = 0.0;
+  for (int c = 0; c < m; ++c) {
+    double s = 0.0;
+    for (int r = 0; r < m; ++r) s += fabs(a[r * m + c]);
+    if (s > best) best = s;
+  }
+  return best;
+}
+static double mat_norm_inf(const double* a, int m) {
+  double best = 0.0;
+  for (int r = 0; r < m; ++r) {
+    double s = 0.0;
+    for (int c = 0; c < m; ++c) s += fabs(a[r * m + c]);
+    if (s > best) best = s;
+  }
+  return best;
+}
+/* c = a b for m x m matrices (c must not alias a or b) */
+static void mat_mul(const double* a, const double* b, double* c, int m) {
+  for (int r = 0; r < m; ++r)
+    for (int col = 0; col < m; ++col) {
+      double s = 0.0;
+      for (int t = 0; t < m; ++t) s += a[r * m + t] * b[t * m + col];
+      c[r * m + col] = s;
+    }
+}
+
+/*
+ * Newton-Schulz pseudo-inverse of the m x m matrix a after `iters` steps, with
+ * the ridge when kappa > 0 (see above).  out is m x m.  Returns 0, or -1 on
+ * bad arguments or allocation failure.
+ */
+int oracle_ns_pinv(const double* a, int m, int iters, double kappa, double* out) {
+  if (m <= 0 || iters < 0) return -1;
+  const size_t mm = (size_t)m * m;
+  double* mat = (double*)malloc(sizeof(double) * mm);
+  double* x = (double*)malloc(sizeof(double) * mm);
+  double* t1 = (double*)malloc(sizeof(double) * mm);
+  double* t2 = (double*)malloc(sizeof(double) * mm);
+  if (!mat || !x || !t1 || !t2) {
+    free(mat); free(x); free(t1); free(t2);
+    return -1;
+  }
+  if (kappa > 0.0) {
+    const double lambda = mat_norm1(a, m) * mat_norm_inf(a, m) / kappa;
+    for (int r = 0; r < m; ++r)
+      for (int c = 0; c < m; ++c) {
+        double s = 0.0;
+        for (int t = 0; t < m; ++t) s += a[t * m + r] * a[t * m + c];
+        mat[r * m + c] = s + (r == c ? lambda : 0.0);
+      }
+  } else {
+    memcpy(mat, a, sizeof(double) * mm);
+  }
+  const double c0 = mat_norm1(mat, m) * mat_norm_inf(mat, m);
+  for (int r = 0; r < m; ++r)
+    for (int c = 0; c < m; ++c) x[r * m + c] = c0 > 0.0 ? mat[c * m + r] / c0 : 0.0;
+  for (int it = 0; it < iters; ++it) {
+    mat_mul(mat, x, t1, m);   /* A X */
+    mat_mul(x, t1, t2, m);    /* X A X */
+    for (size_t e = 0; e < mm; ++e) x[e] = 2.0 * x[e] - t2[e];
+  }
+  if (kappa > 0.0) {
+    /* pinv(A) = X(M) A^T */
+    for (int r = 0; r < m; ++r)
+      for (int c = 0; c < m; ++c) {
+        double s = 0.0;
+        for (int t = 0; t < m; ++t) s += x[r * m + t] * a[c * m + t];
+        out[r * m + c] = s;
+      }
+  } else {
+    memcpy(out, x, sizeof(double) * mm);
+  }
+  free(mat); free(x); free(t1); free(t2);
+  return 0;
+}
+
+/* landmark i of one head: mean of rows floor(i N / m) .. floor((i+1) N / m) - 1 */
+static void landmarks(const double* xh, int64_t N, int64_t D, int m, double* out) {
+  for (int i = 0; i < m; ++i) {
+    const int64_t lo = (int64_t)i * N / m, hi = (int64_t)(i + 1) * N / m;
+    double* oi = out + (int64_t)i * D;
+    for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+    for (int64_t r = lo; r < hi; ++r)
+      for (int64_t d = 0; d < D; ++d) oi[d] += xh[r * D + d];
+    for (int64_t d = 0; d < D; ++d) oi[d] /= (double)(hi - lo);
+  }
+}
+
+/*
+ * Full Nystrom forward.  q [B,Hq,N,D], k and v [B,Hkv,N,D], o [B,Hq,N,D].
+ * Optional intermediates (NULL to skip): qt [B,Hq,m,D], kt [B,Hkv,m,D],
+ * pinv [B,Hq,m,m] (the pseudo-inverse of the landmark softmax), w [B,Hq,m,D]
+ * (softmax(Qt K^T) V).  Returns 0, or -1 on bad sizes / allocation failure.
+ */
+int oracle_nys_fwd(const double* q, const double* k, const double* v,
+                   int B, int Hq, int Hkv, int N, int D, int m, int iters, double kappa,
+                   double scale, double* o, double* qt_out, double* kt_out,
+                   double* pinv_out, double* w_out) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv || m <= 0 || N < m || iters < 0)
+    return -1;
+  const int64_t G = Hq / Hkv, BH = (int64_t)B * Hq, BHk = (int64_t)B * Hkv;
+  const int64_t mD = (int64_t)m * D, mm = (int64_t)m * m;
+  double* qt = (double*)malloc(sizeof(double) * (BH * mD + 1));
+  double* kt = (double*)malloc(sizeof(double) * (BHk * mD + 1));
+  double* pinv = (double*)malloc(sizeof(double) * (BH * mm + 1));
+  double* w = (double*)malloc(sizeof(double) * (BH * mD + 1));
+  double* y = (double*)malloc(sizeof(double) * (BH * mD + 1));
+  int err = (!qt || !kt || !pinv || !w || !y) ? -1 : 0;
+  if (!err) {
+    /* landmarks */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH + BHk; ++bh) {
+      if (bh < BH) landmarks(q + bh * (int64_t)N * D, N, D, m, qt + bh * mD);
+      else landmarks(k + (bh - BH) * (int64_t)N * D, N, D, m, kt + (bh - BH) * mD);
+    }
+    /* landmark softmax A2 = softmax(Qt Kt^T) and its pseudo-inverse */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+      const int64_t b = bh / Hq, h = bh % Hq, hk = b * Hkv + h / G;
+      double* a2 = (double*)malloc(sizeof(double) * mm);
+      if (!a2) {
+#pragma omp atomic write
+        err = -1;
+        continue;
+      }
+      for (int i = 0; i < m; ++i) {
+        row_scores(qt + bh * mD + (int64_t)i * D, kt + hk * mD, m, D, 0, 0, scale, a2 + (int64_t)i * m);
+        row_softmax(a2 + (int64_t)i * m, m);
+      }
+      if (oracle_ns_pinv(a2, m, iters, kappa, pinv + bh * mm)) {
+#pragma omp atomic write
+        err = -1;
+      }
+      free(a2);
+    }
+  }
+  if (!err) {
+    /* W = softmax(Qt K^T) V, one landmark row at a time */
+#pragma omp parallel
+    {
+      double* s = (double*)malloc(sizeof(double) * N);
+      if (!s) {
+#pragma omp atomic write
+        err = -1;
+      }
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t r = 0; r < BH * m; ++r) {
+        if (!s) continue;
+        const int64_t bh = r / m, i = r % m, b = bh / Hq, h = bh % Hq;
+        const int64_t hk = b * Hkv + h / G;
+        const double* vh = v + hk * (int64_t)N * D;
+        row_scores(qt + bh * mD + i * D, k + hk * (int64_t)N * D, N, D, 0, 0, scale, s);
+        row_softmax(s, N);
+        double* wi = w + bh * mD + i * D;
+        for (int64_t d = 0; d < D; ++d) wi[d] = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+          for (int64_t d = 0; d < D; ++d) wi[d] += s[j] * vh[j * D + d];
+      }
+      free(s);
+    }
+  }
+  if (!err) {
+    /* Y = pinv W */
+#pragma omp parallel for schedule(static)
+    for (int64_t bh = 0; bh < BH; ++bh)
+      for (int i = 0; i < m; ++i)
+        for (int64_t d = 0; d < D; ++d) {
+          double s = 0.0;
+          for (int t = 0; t < m; ++t) s += pinv[bh * mm + (int64_t)i * m + t] * w[bh * mD + (int64_t)t * D + d];
+          y[bh * mD + (int64_t)i * D + d] = s;
+        }
+    /* O_r = softmax(q_r Kt^T) Y */
+#pragma omp parallel
+    {
+      double* s = (double*)malloc(sizeof(double) * m);
+      if (!s) {
+#pragma omp atomic write
+        err = -1;
+      }
+#pragma omp for schedule(dynamic, 64)
+      for (int64_t r = 0; r < BH * (int64_t)N; ++r) {
+        if (!s) continue;
+        const int64_t bh = r / N, b = bh / Hq, h = bh % Hq, hk = b * Hkv + h / G;
+        row_scores(q + r * D, kt + hk * mD, m, D, 0, 0, scale, s);
+        row_softmax(s, m);
+        double* orow = o + r * D;
+        for (int64_t d = 0; d < D; ++d) orow[d] = 0.0;
+        for (int t = 0; t < m; ++t)
+          for (int64_t d = 0; d < D; ++d) orow[d] += s[t] * y[bh * mD + (int64_t)t * D + d];
+      }
+      free(s);
+    }
+  }
+  if (!err) {
+    if (qt_out) memcpy(qt_out, qt, sizeof(double) * BH * mD);
+    if (kt_out) memcpy(kt_out, kt, sizeof(double) * BHk * mD);
+    if (pinv_out) memcpy(pinv_out, pinv, sizeof(double) * BH * mm);
+    if (w_out) memcpy(w_out, w, sizeof(double) * BH * mD);
+  }
+  free(qt); free(kt); free(pinv); free(w); free(y);
+  return err;
+}

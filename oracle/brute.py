@@ -125,3 +125,74 @@ def brute_stj_fwd(q, k, v, B, Hq, Hkv, N, D, causal, scale, order, steps):
                     o[base + d] = math.fsum(w[t] * _row(v, ks, b, hk, j)[d]
                                             for t, j in enumerate(keys))
     return o, pole
+
+
+def _matmul(a, b):
+    """Product of two matrices held as lists of rows (math.fsum per entry)."""
+    cols = list(zip(*b))
+    return [[math.fsum(x * y for x, y in zip(r, c)) for c in cols] for r in a]
+
+
+def _softmax(row):
+    mx = max(row)
+    e = [math.exp(x - mx) for x in row]
+    t = math.fsum(e)
+    return [x / t for x in e]
+
+
+def brute_nys_fwd(q, k, v, B, Hq, Hkv, N, D, m, iters, kappa, scale):
+    """Nystrom attention (FlashNystrom page, "Scope" and "Configuration"):
+    landmarks are the means of the m segments floor(iN/m)..floor((i+1)N/m)-1,
+    O = softmax(s Q Kt^T) pinv(softmax(s Qt Kt^T)) softmax(s Qt K^T) V with
+    pinv from `iters` Newton-Schulz steps X <- 2X - X A X started at
+    A^T / (|A|_1 |A|_inf), on A^T A + lambda I (lambda = |A|_1 |A|_inf / kappa)
+    followed by a product with A^T when kappa > 0.  Returns o as a flat list."""
+    G = Hq // Hkv
+    qs, ks = (B, Hq, N, D), (B, Hkv, N, D)
+    o = [0.0] * (B * Hq * N * D)
+
+    def pool(flat, shape, b, h):
+        out = []
+        for i in range(m):
+            lo, hi = i * N // m, (i + 1) * N // m
+            rows = [_row(flat, shape, b, h, r) for r in range(lo, hi)]
+            out.append([math.fsum(r[d] for r in rows) / (hi - lo) for d in range(D)])
+        return out
+
+    def norms(a):
+        n1 = max(math.fsum(abs(a[r][c]) for r in range(len(a))) for c in range(len(a)))
+        ninf = max(math.fsum(abs(x) for x in r) for r in a)
+        return n1 * ninf
+
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // G
+            Q = [_row(q, qs, b, h, i) for i in range(N)]
+            K = [_row(k, ks, b, hk, j) for j in range(N)]
+            V = [_row(v, ks, b, hk, j) for j in range(N)]
+            Qt, Kt = pool(q, qs, b, h), pool(k, ks, b, hk)
+            scores = lambda X, Y: [[scale * math.fsum(a * c for a, c in zip(x, y)) for y in Y]
+                                   for x in X]
+            A1 = [_softmax(r) for r in scores(Q, Kt)]
+            A2 = [_softmax(r) for r in scores(Qt, Kt)]
+            A3 = [_softmax(r) for r in scores(Qt, K)]
+            A2T = [list(c) for c in zip(*A2)]
+            if kappa > 0:
+                lam = norms(A2) / kappa
+                M = _matmul(A2T, A2)
+                for i in range(m):
+                    M[i][i] += lam
+            else:
+                M = A2
+            c0 = norms(M)
+            X = [[x / c0 for x in c] for c in zip(*M)]
+            for _ in range(iters):
+                XAX = _matmul(X, _matmul(M, X))
+                X = [[2.0 * x - y for x, y in zip(rx, ry)] for rx, ry in zip(X, XAX)]
+            P = _matmul(X, A2T) if kappa > 0 else X
+            Y = _matmul(P, _matmul(A3, V))
+            Oh = _matmul(A1, Y)
+            for i in range(N):
+                base = _idx(qs, b, h, i)
+                o[base:base + D] = Oh[i]
+    return o
