@@ -30,6 +30,7 @@ SIGNATURES = {
                          _I),
     "attn_fwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_stieltjes_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
+    "attn_nystrom_fwd": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P], _I),
     "attn_bwd_deterministic": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
                                 _P], _I),
     "attn_bwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P], _I),
@@ -120,6 +121,14 @@ def attn_stieltjes_fwd(q, k, v, o, pole, B, Hq, Hkv, N, D, causal, scale, order,
     return load().attn_stieltjes_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(pole), B, Hq, Hkv,
                                      N, D, int(bool(causal)), float(scale), int(order),
                                      int(newton_steps), _stream_handle(stream))
+
+
+def attn_nystrom_fwd(q, k, v, o, B, Hq, Hkv, N, D, num_landmarks, newton_iters, kappa, scale,
+                     stream=None):
+    """Raw call of the Nystrom attention forward; returns the status code."""
+    return load().attn_nystrom_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, N, D,
+                                   int(num_landmarks), int(newton_iters), float(kappa),
+                                   float(scale), _stream_handle(stream))
 
 
 def attn_bwd_deterministic(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq,
@@ -273,3 +282,24 @@ def stieltjes_attn(q, k, v, causal=False, scale=None, order=4, newton_steps=3, s
     if st != ATTN_OK:
         raise AttnError(st, "attn_stieltjes_fwd")
     return o, pole
+
+
+def nystrom_attn(q, k, v, num_landmarks=64, newton_iters=6, kappa=5.0, scale=None, stream=None):
+    """Nystrom attention (FlashNystrom page) for bf16 CUDA tensors q [B,Hq,N,D],
+    k/v [B,Hkv,N,D]: segment-mean landmarks, Newton-Schulz pseudo-inverse with
+    the Tikhonov ridge kappa (0 = none).  The defaults are the page's
+    (64 landmarks, 6 iterations, kappa 5)."""
+    import torch
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    _check(q, (B, Hq, N, D), "q", torch.bfloat16)
+    _check(k, (B, Hkv, N, D), "k", torch.bfloat16)
+    _check(v, (B, Hkv, N, D), "v", torch.bfloat16)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    st = attn_nystrom_fwd(q, k, v, o, B, Hq, Hkv, N, D, num_landmarks, newton_iters, kappa,
+                          scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_nystrom_fwd")
+    return o

@@ -85,12 +85,13 @@ int device_sm_count(int dev) {
 }
 
 // 3-D map over a contiguous bf16 (or fp16) [BH, N, D] tensor: dims (D, N, BH), box
-// (64, 128, 1), 128-byte swizzle.  Rows past N inside a (batch, head) plane
+// (64, box_rows, 1) (128 rows unless a caller asks for fewer), 128-byte swizzle.  Rows past N inside a (batch, head) plane
 // read as zero, so a ragged tail never reads the next head.
-int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16) {
+int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16,
+                    int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         3, const_cast<void*>(base), dims,

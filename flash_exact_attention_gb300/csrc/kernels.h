@@ -25,6 +25,51 @@ struct FwdParams {
   int steps;
 };
 
+// Nystrom attention forward (six kernels; nys_kernel.cuh).  Landmark rows are
+// padded to mp (m rounded up to a multiple of 16, at least 16) wherever they
+// are a tensor-core operand dimension.
+struct NysParams {
+  const void* q;        // bf16 [B, Hq, N, D]
+  const void* k;        // bf16 [B, Hkv, N, D]
+  void* o;              // bf16 [B, Hq, N, D]
+  int B, Hq, Hkv, N, G;
+  int m, mp;            // landmarks, and m padded for the tensor cores
+  int iters;            // Newton-Schulz steps
+  float kappa;          // ridge target condition number (0 = no ridge)
+  float scale;          // score scale
+  float scale_log2;     // scale * log2(e)
+  int num_kv_tiles;     // ceil(N / 128)
+  // Q pooling: partial segment sums [B*Hq, m, pool_splits, D]
+  int pool_splits;
+  float* pool_part;
+  float* qt32;          // fp32 [B*Hq, m, D]: Qt
+  // bf16 hi/lo pairs (x = hi + lo, rows >= m zero) of the tensor-core operands:
+  uint16_t* qt16;       // [B*Hq, 2, 128, D]: Qt as two 128-row A tiles
+  uint16_t* kt16;       // [B*Hkv, 2, mp, D]: Kt
+  uint16_t* y16;        // [B*Hq, 2, mp, D]: Y = pinv(A2) W
+  // split-key pass: chunk c of a head covers key tiles [c*kv_tpc, (c+1)*kv_tpc)
+  int kv_chunks, kv_tpc;
+  float* kv_o;          // fp32 [B*Hq, kv_chunks, m, D]: unnormalised partial W
+  float* kv_ml;         // fp32 [B*Hq, kv_chunks, m, 2]: row max (log2 units), row sum
+  float* w;             // fp32 [B*Hq, m, D]: W = softmax(scale Qt K^T) V
+  // K segment sums from the split-key pass: slot k of segment i holds the sum
+  // over its rows in chunk floor(first row of i / chunk rows) + k
+  int kparts;
+  float* kpart;         // fp32 [B*Hkv, m, kparts, D]
+  int out_ctas;         // persistent CTAs of the output pass
+  uint64_t timeout_ns;
+  unsigned int* err;
+};
+
+// Enqueues the six Nystrom kernels (tq, to: q and o; tk, tv: k and v; tqt,
+// tkt, ty: the landmark and Y operand tiles in scratch).
+cudaError_t launch_nys_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tqt, const CUtensorMap& tkt, const CUtensorMap& ty,
+                           const CUtensorMap& to, const NysParams& p, cudaStream_t stream);
+cudaError_t launch_nys_d128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tqt, const CUtensorMap& tkt, const CUtensorMap& ty,
+                            const CUtensorMap& to, const NysParams& p, cudaStream_t stream);
+
 // Backward parameters of the main kernel (everything but the tensor maps).
 struct BwdParams {
   void* dk;             // bf16 [B, Hkv, N, D]
@@ -117,7 +162,8 @@ cudaError_t launch_bwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
 int validate_shape(int B, int Hq, int Hkv, int N, int D, float scale);
 int device_setup(int* dev_out, unsigned int** err_out);
 int device_sm_count(int dev);
-int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16 = false);
+int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16 = false,
+                    int box_rows = 128);
 int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH);
 uint64_t wait_timeout_ns();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -1,0 +1,41 @@
+// Nystrom attention forward kernels for head dim 64.
+#include "nys_kernel.cuh"
+
+namespace attn {
+
+cudaError_t launch_nys_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tqt, const CUtensorMap& tkt, const CUtensorMap& ty,
+                          const CUtensorMap& to, const NysParams& p, cudaStream_t stream) {
+  constexpr int D = 64;
+  const int BH = p.B * p.Hq;
+  cudaError_t e;
+  nys_pool_kernel<D><<<dim3(p.pool_splits, p.m, BH), 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  nys_qt_kernel<D><<<dim3(128, BH), D, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(nys_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           NysKvCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  nys_kv_kernel<D><<<dim3(p.kv_chunks, BH), NysKvCfg<D>::kThreads, NysKvCfg<D>::kSmemBytes,
+                     stream>>>(tqt, tk, tv, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  nys_merge_kernel<D><<<dim3(p.m, BH), 4 * D, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(nys_lmy_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           NysLyCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  nys_lmy_kernel<D><<<BH, NysLyCfg<D>::kThreads, NysLyCfg<D>::kSmemBytes, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  e = cudaFuncSetAttribute(nys_out_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           NysOutCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  nys_out_kernel<D><<<p.out_ctas, NysOutCfg<D>::kThreads, NysOutCfg<D>::kSmemBytes, stream>>>(
+      tq, tkt, ty, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -40,6 +40,23 @@ def make_inputs_f16(B, Hq, Hkv, N, D, seed, with_do=False):
     return out
 
 
+def make_inputs_clustered(B, Hq, Hkv, N, D, seed, clusters=8, amp=1.0, noise=0.5):
+    """bf16 bit arrays whose Q and K rows come in `clusters` contiguous runs:
+    row r of a (batch, head) plane is amp * c_{floor(r * clusters / N)} + noise * z_r,
+    centres c and z iid N(0,1); V iid N(0,1).  Neighbouring tokens that look
+    alike make the landmark means large and the landmark softmaxes peaked, unlike
+    iid rows whose segment means shrink towards zero."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    seg = (np.arange(N) * clusters) // N
+    for name, h in (("q", Hq), ("k", Hkv)):
+        c = rng.standard_normal((B, h, clusters, D), dtype=np.float32)
+        z = rng.standard_normal((B, h, N, D), dtype=np.float32)
+        out[name] = f32_to_bf16_bits(amp * c[:, :, seg, :] + noise * z)
+    out["v"] = f32_to_bf16_bits(rng.standard_normal((B, Hkv, N, D), dtype=np.float32))
+    return out
+
+
 def to_torch_bf16(bits):
     """View uint16 bf16 bit patterns as a CPU torch.bfloat16 tensor (no rounding)."""
     import torch

@@ -122,6 +122,32 @@ int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int newton_steps, void* stream);
 
 /*
+ * Nystrom attention forward (bf16 in and out).  FlashNystrom page, "Scope":
+ *     O = softmax(s Q Kt^T) . pinv(softmax(s Qt Kt^T)) . softmax(s Qt K^T) . V
+ * per (batch, query head), s = scale, every softmax over its rows.  Qt and Kt
+ * are the m = num_landmarks landmarks: landmark i is the mean of rows
+ * floor(i N / m) .. floor((i+1) N / m) - 1 of Q (of that query head) and of K
+ * (of its key/value head h / (Hq / Hkv)).  pinv is newton_iters unrolled
+ * Newton-Schulz steps X <- 2X - X A X from X = A^T / (|A|_1 |A|_inf), in fp32;
+ * with kappa > 0 ("Configuration": the Tikhonov ridge) they run on
+ * A^T A + lambda I, lambda = |A|_1 |A|_inf / kappa, and pinv(A) = X A^T;
+ * kappa = 0 runs them on A itself.  No causal mask, no value convolution.
+ *   q, o : bf16 [B, Hq, N, D];  k, v : bf16 [B, Hkv, N, D]  (device, 16-byte
+ *   aligned, contiguous).  D in {64, 128}; 1 <= num_landmarks <= 64 (larger:
+ *   ATTN_ERR_UNSUPPORTED); N >= num_landmarks; 0 <= newton_iters <= 100;
+ *   kappa finite and >= 0; B * (Hq + Hkv) <= 65535.  B * Hq == 0 returns
+ *   ATTN_OK without launching.
+ * Landmarks, the landmark softmax, W = softmax(s Qt K^T) V and pinv(A) W are
+ * fp32; Qt, Kt, P and pinv(A) W enter the tensor cores as bf16.  Scratch of
+ * about (B*Hq + B*Hkv) * m * D * 4 * splits + B*Hq*(chunks*m*(D+2)*4 + ...)
+ * bytes is taken with cudaMallocAsync / cudaFreeAsync on `stream`.  Five
+ * kernel launches.
+ */
+int attn_nystrom_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                     int Hkv, int N, int D, int num_landmarks, int newton_iters, float kappa,
+                     float scale, void* stream);
+
+/*
  * Deterministic backward (bf16): the arguments, layouts and error codes of
  * attn_bwd, with results that are bitwise identical from run to run.
  * attn_bwd adds each key tile's fp32 dQ partial into an accumulator in
