@@ -76,7 +76,8 @@ int nys_entry(const void* q, const void* k, const void* v, void* o, int B, int H
     p.kv_tpc = (int)tpc;
     p.kv_chunks = (int)((T + tpc - 1) / tpc);
   }
-  // Chunks that one landmark segment meets, at most.
+  // K-sum slots of a segment: the chunks one landmark segment meets, at most,
+  // times the row shares of a key tile (4 at D = 64, 2 at D = 128).
   {
     const long long rows = (long long)p.kv_tpc * 128;
     long long parts = 1;
@@ -85,7 +86,7 @@ int nys_entry(const void* q, const void* k, const void* v, void* o, int B, int H
       const long long c = (hi - 1) / rows - lo / rows + 1;
       if (c > parts) parts = c;
     }
-    p.kparts = (int)parts;
+    p.kparts = (int)parts * (D == 64 ? 4 : 2);
   }
   p.out_ctas = (int)(BH * T < sms ? BH * T : sms);
   p.timeout_ns = wait_timeout_ns();
@@ -134,7 +135,10 @@ int nys_entry(const void* q, const void* k, const void* v, void* o, int B, int H
       encode_tile_map(&ty, p.y16, D, 2 * p.mp, (int)BH, false, p.mp) != ATTN_OK) {
     st = ATTN_ERR_CUDA;
   } else {
-    cudaError_t e = (D == 64) ? launch_nys_d64(tq, tk, tv, tqt, tkt, ty, to, p, s)
+    // K-sum slots that no (chunk, share) pair writes must read as zero
+    cudaError_t e = cudaMemsetAsync(p.kpart, 0, b_kpart, s);
+    if (e == cudaSuccess)
+      e = (D == 64) ? launch_nys_d64(tq, tk, tv, tqt, tkt, ty, to, p, s)
                               : launch_nys_d128(tq, tk, tv, tqt, tkt, ty, to, p, s);
     st = e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }

@@ -26,7 +26,8 @@
 //   6 nys_out_kernel    persistent over 128-row query tiles: S = Q Kt^T
 //                       (tcgen05, N = mp), softmax over the m landmarks,
 //                       O = P Y (tcgen05, K = mp), bf16 out through a swizzled
-//                       staging tile and a TMA store
+//                       staging tile and a TMA store; two warp groups take
+//                       alternate tiles
 //
 // HBM traffic: Q twice (kernels 1 and 6), K and V once (kernel 3), O once.
 //
@@ -116,10 +117,15 @@ __global__ void __launch_bounds__(D) nys_qt_kernel(const NysParams p) {
   float x = 0.f;
   if (i < m) {
     const float* pq = p.pool_part + ((size_t)bh * m + i) * S * D + d;
-    float s = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < S; ++k) s += pq[(size_t)k * D];
-    x = s / (float)(seg_lo(i + 1, p.N, m) - seg_lo(i, p.N, m));
+    float s0 = 0.f, s1 = 0.f;  // two chains; the unrolled loads go out together
+    int k = 0;
+#pragma unroll 4
+    for (; k + 1 < S; k += 2) {
+      s0 += pq[(size_t)k * D];
+      s1 += pq[(size_t)(k + 1) * D];
+    }
+    if (k < S) s0 += pq[(size_t)k * D];
+    x = (s0 + s1) / (float)(seg_lo(i + 1, p.N, m) - seg_lo(i, p.N, m));
     p.qt32[((size_t)bh * m + i) * D + d] = x;
   }
   uint16_t* q16 = p.qt16 + (size_t)bh * 2 * 128 * D + (size_t)i * D + d;
@@ -257,7 +263,8 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
   const int bhk = b * p.Hkv + h / p.G;
 
   // Qt from its fp32 copy, Kt from the key-chunk partial sums of its segments
-  // (chunks c_first(i) .. c_last(i) wrote slots 0 .. c_last - c_first)
+  // (chunk c_first(i) + k, share s of its tiles wrote slot k * shares + s;
+  // slots of no (chunk, share) pair stay zero)
   const long long chunk_rows = (long long)p.kv_tpc * 128;
 #pragma unroll 4
   for (int idx = t; idx < D * mp; idx += 512) {
@@ -266,11 +273,17 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
     if (i < m) {
       qv = p.qt32[((size_t)bh * m + i) * D + d];
       const long long lo = seg_lo(i, p.N, m), hi = seg_lo(i + 1, p.N, m);
-      const int parts = (int)((hi - 1) / chunk_rows - lo / chunk_rows) + 1;
+      const int parts = ((int)((hi - 1) / chunk_rows - lo / chunk_rows) + 1) * (4 / (D / 64));
       const float* pk = p.kpart + (((size_t)bhk * m + i) * P) * D + d;
-      float s = 0.f;
-      for (int k = 0; k < parts; ++k) s += pk[(size_t)k * D];
-      kv = s / (float)(hi - lo);
+      float s0 = 0.f, s1 = 0.f;  // two chains; the unrolled loads go out together
+      int k = 0;
+#pragma unroll 4
+      for (; k + 1 < parts; k += 2) {
+        s0 += pk[(size_t)k * D];
+        s1 += pk[(size_t)(k + 1) * D];
+      }
+      if (k < parts) s0 += pk[(size_t)k * D];
+      kv = (s0 + s1) / (float)(hi - lo);
     }
     qtT[d * LD + i] = qv;
     ktT[d * LD + i] = kv;
@@ -401,18 +414,19 @@ struct NysKvCfg {
   static constexpr int kNumBars = 1 + 2 * kSlots + 6;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "more shared memory than one CTA may have");
-  static constexpr int kThreads = 192;  // 4 softmax warps, producer, MMA
+  static constexpr int kThreads = 256;  // softmax warps 0-1, K-sum warps 2-3 and 6-7, producer, MMA
   static constexpr uint32_t kTmemCols = 512;  // S0, S1 (128 each), O (D)
 };
 
 // grid (kv_chunks, B*Hq).  Warps 0-1: thread = landmark row = TMEM lane (rows
 // >= m are the zero padding of the A tile; m <= 64, so warps 2-3 hold none);
-// warps 2-3: in the CTA of the first query head of each key/value head, the
-// K row sums of each landmark segment, read from the K tiles in shared memory
-// (warp 2 columns 0-63, warp 3 columns 64-127), written per (segment, chunk);
-// warp 4: TMA producer (Qt once, K_j and V_j through the ring); warp 5: MMA.
-// A ring slot is free again once the MMA has read it and warps 2-3 have
-// passed it.
+// warp 4: TMA producer (Qt once, K_j and V_j through the ring); warp 5: MMA;
+// K-sum warps 2, 3, 6, 7: in the CTA of the first query head of each
+// key/value head, the K row sums of each landmark segment, read from the K
+// tiles in shared memory and written per (segment, chunk, warp): K-sum warp w
+// (0-3) takes the 64-column box w % (D / 64) of the rows in its share
+// w / (D / 64) of each tile.  A ring slot is free again once the MMA has read
+// it and the four K-sum warps have passed it.
 // Order of the tensor work: S_0, S_1, O += P_0 V_0, S_2, O += P_1 V_1, ...;
 // S_j overwrites the TMEM columns that P_{j-2} occupied only after the
 // (in-order) O += P_{j-2} V_{j-2} was issued.
@@ -420,7 +434,7 @@ struct NysKvCfg {
 // P V has completed) only when the tile max exceeds the max in use by more
 // than 8 (log2 units), so the weights in use stay below 2^8.
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(256, 1)
     nys_kv_kernel(const __grid_constant__ CUtensorMap tm_qt, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const NysParams p) {
   using Cfg = NysKvCfg<D>;
@@ -450,7 +464,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bar_q(), 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 3);  // MMA commit + warps 2 and 3
+      mbar_init(bar_empty(s), 5);  // MMA commit + the four K-sum warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_s(b), 1);
@@ -554,10 +568,13 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(bar_done());
       if (!ok) mbar_wait_drain_inl(bar_done(), 0, wc);
     }
-  } else if (warp >= 2) {
+  } else if (warp == 2 || warp == 3 || warp >= 6) {
     // ------------------------------------------------------------ K segment sums
-    const int box = warp - 2;
-    const bool pools = (h % p.G == 0) && box < Cfg::kBoxes;
+    constexpr int kShares = 4 / Cfg::kBoxes;  // row shares of a tile
+    const int ks = warp < 6 ? warp - 2 : warp - 4;  // 0..3
+    const int box = ks % Cfg::kBoxes, share = ks / Cfg::kBoxes;
+    const int r_lo = share * (128 / kShares), r_hi = r_lo + 128 / kShares;
+    const bool pools = h % p.G == 0;
     const long long chunk_rows = (long long)p.kv_tpc * 128;
     float s0 = 0.f, s1 = 0.f;
     int seg = -1;
@@ -566,7 +583,7 @@ __global__ void __launch_bounds__(192, 1)
       if (seg >= 0) {
         const int k = chunk - (int)(seg_lo(seg, p.N, m) / chunk_rows);
         float2* dst = reinterpret_cast<float2*>(
-            p.kpart + (((size_t)bhk * m + seg) * p.kparts + k) * D + box * 64);
+            p.kpart + (((size_t)bhk * m + seg) * p.kparts + k * kShares + share) * D + box * 64);
         dst[lane] = make_float2(s0, s1);
       }
       s0 = s1 = 0.f;
@@ -578,9 +595,9 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) break;
       if (pools && (it & 1) == 0) {
         const long long g0 = (long long)(j0 + it / 2) * 128;
-        const int rows = (int)min(128LL, (long long)p.N - g0);
-        if (seg < 0) {
-          seg = (int)(((g0 + 1) * m - 1) / p.N);  // the segment holding row g0
+        const int rows = (int)min((long long)r_hi, (long long)p.N - g0);  // this share's end
+        if (seg < 0 && r_lo < rows) {
+          seg = (int)(((g0 + r_lo + 1) * m - 1) / p.N);  // the segment holding row g0 + r_lo
           next_lo = seg_lo(seg + 1, p.N, m);
         }
         const uint32_t base = slot(s) + box * Cfg::kBoxBytes + (uint32_t)(lane & 3) * 4u;
@@ -592,9 +609,11 @@ __global__ void __launch_bounds__(192, 1)
                        : "r"(base + (uint32_t)r * 128u + (uint32_t)(((lane >> 2) ^ (r & 7)) << 4)));
           return v;
         };
-        int r = 0;
+        int r = r_lo;
         while (r < rows) {
-          if (g0 + r >= next_lo) {
+          // segments may also have ended in rows of the other shares: each
+          // one passed gets its (possibly empty) sum written
+          while (g0 + r >= next_lo) {
             flush();
             ++seg;
             next_lo = seg_lo(seg + 1, p.N, m);
@@ -780,19 +799,22 @@ struct NysOutCfg {
   static constexpr int kNumBars = 2 * kStages + 11;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "more shared memory than one CTA may have");
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;  // two groups of 4 softmax warps, producer, MMA
   // S0, S1 (64 columns each), O0, O1 (D each)
   static constexpr uint32_t kTmemCols = (128 + 2 * D) <= 256 ? 256 : 512;
 };
 
 // Persistent: CTA c owns query tiles [c*W/G, (c+1)*W/G) of the B*Hq*T tiles,
-// head-major, so consecutive tiles mostly share Kt and Y.  Warps 0-3: thread =
-// query row = TMEM lane (softmax over the landmarks, then the epilogue of the
-// previous tile); warp 4: TMA (Kt and Y on a head change, Q tiles through a
-// ring); warp 5: MMA, in the order S_0, S_1, O_0 = P_0 Y, S_2, O_1 = P_1 Y, ...
-// with the previous head's last P Y issued before Kt and Y are replaced.
+// head-major, so consecutive tiles mostly share Kt and Y.  Warps 0-3 and 4-7
+// are two groups that take the CTA's tiles in turn (group g the tiles t with
+// t % 2 == g, TMEM buffers S_g, O_g, staging tile g): thread = query row =
+// TMEM lane, softmax over the landmarks, then the epilogue of the same tile,
+// while the other group works on its neighbour.  Warp 8: TMA (Kt and Y on a
+// head change, Q tiles through a ring); warp 9: MMA, in the order S_0, S_1,
+// O_0 = P_0 Y, S_2, O_1 = P_1 Y, ... with the previous head's last P Y issued
+// before Kt and Y are replaced.
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     nys_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kt,
                    const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_o,
                    const NysParams p) {
@@ -836,8 +858,8 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
-  if (warp == 4 && lane == 0) {
+  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kt);
     tma_prefetch_desc(&tm_y);
@@ -855,7 +877,7 @@ __global__ void __launch_bounds__(192, 1)
   const int m = p.m, mp = p.mp;
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int cur = -1;
@@ -892,7 +914,7 @@ __global__ void __launch_bounds__(192, 1)
         if (nky > 0) mbar_wait_drain_inl(bar_kyf(), (nky - 1) & 1u, wc);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = make_idesc_bf16(128, (uint32_t)mp, 0, 0);
@@ -957,25 +979,28 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int g = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t bar_id = 1u + (uint32_t)g;  // named barrier of the group (128 threads)
+    const bool leader = threadIdx.x == (unsigned)(g * 128);
     const float c = p.scale_log2;
-    bool ok = true;
-    float linv_prev = 0.f;
-    // O_u / l -> bf16 -> staging tile u % 2 (128-byte swizzle, the TMA layout)
-    // -> TMA store, which leaves out rows past N.  Thread 0 first waits until
-    // the store issued from that tile two epilogues ago has read it.
-    const uint32_t st_row = sbase + Cfg::kStOff + (uint32_t)row * 128u;
+    const uint32_t tS = tmem_base + lane_off + (uint32_t)(g * 64);
+    const uint32_t tO = tmem_base + lane_off + 128u + (uint32_t)(g * D);
+    // staging tile g, row `row` (128-byte swizzle, the TMA layout)
+    const uint32_t st_base = sbase + Cfg::kStOff + (uint32_t)g * Cfg::kTileBytes;
+    const uint32_t st_row = st_base + (uint32_t)row * 128u;
+    // O_u / l -> bf16 -> staging tile -> TMA store (rows past N are left out).
+    // The leader first waits until its previous store has read the tile; every
+    // wait outcome is ANDed over the group's warps at its named barrier, so that
+    // they leave together.
     auto epilogue = [&](int u, float linv) -> bool {
-      const int bb = u & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait_inl(bar_of(bb), (uint32_t)(u >> 1) & 1u, wc));
-      if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      if (!named_bar_and(1, 128, got)) return false;
-      const uint32_t st_tile = (uint32_t)(u & 1) * Cfg::kTileBytes;
+      const bool got = __all_sync(0xffffffffu, mbar_wait_inl(bar_of(g), (uint32_t)(u >> 1) & 1u, wc));
+      if (leader) bulk_wait_read_all();
+      if (!named_bar_and(bar_id, 128, got)) return false;
       tc_fence_after();
       const long long w = w0 + u;
       const int bh = (int)(w / T), qt = (int)(w % T);
-      const uint32_t tO = tmem_base + lane_off + 128u + (uint32_t)(bb * D);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t r[32];
@@ -988,7 +1013,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t x2 = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * linv, __uint_as_float(r[8 * v + 5]) * linv);
           const uint32_t x3 = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * linv, __uint_as_float(r[8 * v + 7]) * linv);
           const int chunk = (q & 1) * 4 + v;  // 16-byte chunk of the 128-byte row
-          const uint32_t addr = st_row + st_tile + (uint32_t)(q >> 1) * Cfg::kBoxBytes +
+          const uint32_t addr = st_row + (uint32_t)(q >> 1) * Cfg::kBoxBytes +
                                 (uint32_t)((chunk ^ (row & 7)) * 16);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x0), "r"(x1),
                        "r"(x2), "r"(x3)
@@ -997,25 +1022,22 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_oe(bb));
+      if (lane == 0) mbar_arrive(bar_oe(g));
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 0) {
-        for (int c = 0; c < Cfg::kBoxes; ++c)
-          tma_store_3d(&tm_o, sbase + Cfg::kStOff + st_tile + c * Cfg::kBoxBytes, c * 64, qt * 128,
-                       bh);
+      named_bar_sync(bar_id, 128);
+      if (leader) {
+        for (int cb = 0; cb < Cfg::kBoxes; ++cb)
+          tma_store_3d(&tm_o, st_base + cb * Cfg::kBoxBytes, cb * 64, qt * 128, bh);
         bulk_commit();
       }
       return true;
     };
-    // The four warps meet at named barrier 1 around the staging tile; every
-    // wait outcome is ANDed over them there first, so that they leave together.
-    for (int t = 0; t < nt && ok; ++t) {
-      const int bb = t & 1;
-      ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait_inl(bar_s(bb), (uint32_t)(t >> 1) & 1u, wc)));
+    bool ok = true;
+    for (int t = g; t < nt && ok; t += 2) {
+      ok = named_bar_and(bar_id, 128,
+                         __all_sync(0xffffffffu, mbar_wait_inl(bar_s(g), (uint32_t)(t >> 1) & 1u, wc)));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem_base + lane_off + (uint32_t)(bb * 64);
       float x[64];
       {
         uint32_t r[4][16];
@@ -1046,17 +1068,15 @@ __global__ void __launch_bounds__(192, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p(bb));
-      if (t > 0 && !(ok = epilogue(t - 1, linv_prev))) break;
-      linv_prev = 1.f / l;
+      if (lane == 0) mbar_arrive(bar_p(g));
+      ok = epilogue(t, 1.f / l);
     }
-    if (ok && nt > 0) epilogue(nt - 1, linv_prev);
-    if (threadIdx.x == 0) bulk_wait_all();
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
