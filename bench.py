@@ -66,6 +66,14 @@ def _measured_peaks():
     return 1900.0, 1700.0, "fallback"
 
 
+def _measured_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
 def _kernel_source_hash(names):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flash_exact_attention_gb300", "csrc")
@@ -396,6 +404,8 @@ def run_native(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if rank == 0 and not args.no_next_rows:
+        result["next_rows"] = next_rows(args.seed)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.workload, has_bwd, args.cpu_seconds)
     if dist is not None:
@@ -403,6 +413,109 @@ def run_native(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def _time_ms(torch, fn, warm=3, reps=10):
+    """Mean device time of fn() over `reps` back-to-back calls (CUDA events on
+    the current stream), after `warm` untimed calls."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def next_rows(seed):
+    """The widened rows, each timed on its own page's workload (synthetic
+    inputs of that shape), outside the headline step's timed region:
+      - Nystrom forward, bound by HBM: algorithmic bytes are Q twice (landmark
+        pooling, output pass), K, V and O once;
+      - Stieltjes forward, bound by the tensor cores: steps + 2 QK^T sweeps and
+        one P.V per tile pair;
+      - the deterministic backward, bound by the tensor cores (7 MMAs per tile
+        pair counted as the 2.5x-forward convention's 5)."""
+    import torch
+
+    from flash_exact_attention_gb300 import binding
+    from flash_exact_attention_gb300.synth import make_inputs, scale_for, to_torch_bf16
+
+    hbm, hbm_src = _measured_hbm()
+    peak_burst, _, peak_src = _measured_peaks()
+    rows = {}
+
+    def dev_inputs(B, Hq, Hkv, N, D, with_do=False):
+        x = make_inputs(B, Hq, Hkv, N, D, seed, with_do=with_do)
+        return {n: to_torch_bf16(a).to("cuda") for n, a in x.items()}
+
+    # Nystrom: the page's high batch x head shape and its long-context shape.
+    for name, (B, H, N, D, m) in (("nystrom_b4_h16_n131072_d128_m64", (4, 16, 131072, 128, 64)),
+                                  ("nystrom_b1_h4_n2097152_d64_m32", (1, 4, 2097152, 64, 32))):
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        q, k, v = (torch.randn(B, H, N, D, device="cuda", generator=g).to(torch.bfloat16)
+                   for _ in range(3))
+        ms = _time_ms(torch, lambda: binding.nystrom_attn(q, k, v, num_landmarks=m,
+                                                          newton_iters=6, kappa=5.0))
+        st = binding.attn_device_status()
+        if st:
+            raise binding.AttnError(st, name)
+        nbytes = 5 * B * H * N * D * 2
+        gbs = nbytes / ms / 1e6
+        rows[name] = {
+            "workload": "Nystrom forward B=%d H=%d N=%d D=%d m=%d, 6 Newton-Schulz steps, "
+                        "kappa 5 (iid N(0,1) bf16)" % (B, H, N, D, m),
+            "metric": "forward latency", "value": round(ms, 4), "unit": "ms",
+            "higher_is_better": False, "launches": 6,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "traffic": None,
+                         "algorithmic_bytes": nbytes,
+                         "peak_source": "%s copy bandwidth" % hbm_src,
+                         "timed_as": "whole attn_nystrom_fwd call (memset + 6 kernels)"}}
+        del q, k, v
+        torch.cuda.empty_cache()
+
+    # Stieltjes attention, order 4, the page's three Newton steps.
+    B, H, N, D = 2, 16, 8192, 128
+    t = dev_inputs(B, H, H, N, D)
+    ms = _time_ms(torch, lambda: binding.stieltjes_attn(t["q"], t["k"], t["v"], order=4,
+                                                        newton_steps=3))
+    st = binding.attn_device_status()
+    if st:
+        raise binding.AttnError(st, "stieltjes")
+    att = 4.0 * B * H * N * N * D / ms / 1e9
+    tensor = att / 2 * (3 + 2 + 1)
+    rows["stieltjes_b2_h16_n8192_d128_q4"] = {
+        "workload": "Stieltjes forward B=2 H=16 N=8192 D=128, order 4, 3 Newton steps",
+        "metric": "attention TFLOPS (4 B H N^2 D per call)", "value": round(att, 1),
+        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
+        "roofline": {"bound": "tensor", "achieved": round(tensor, 1), "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": round(tensor / peak_burst, 4), "traffic": None,
+                     "algorithmic_flops_per_launch": 2.0 * B * H * N * N * D * 6,
+                     "peak_source": "%s bf16 burst" % peak_src}}
+
+    # Deterministic backward on the headline shape.
+    t = dev_inputs(B, H, H, N, D, with_do=True)
+    o, lse = binding.flash_attn(t["q"], t["k"], t["v"])
+    ms = _time_ms(torch, lambda: binding.flash_attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"],
+                                                        deterministic=True))
+    st = binding.attn_device_status()
+    if st:
+        raise binding.AttnError(st, "deterministic backward")
+    tf = 2.5 * 4.0 * B * H * N * N * D / ms / 1e9
+    rows["bwd_deterministic_b2_h16_n8192_d128"] = {
+        "workload": "deterministic backward B=2 H=16 N=8192 D=128 non-causal",
+        "metric": "backward TFLOPS (2.5x forward FLOPs)", "value": round(tf, 1),
+        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 3,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4), "traffic": None,
+                     "peak_source": "%s bf16 burst" % peak_src}}
+    del t, o, lse
+    torch.cuda.empty_cache()
+    return rows
 
 
 # Kernels the backward launches per call, and whether a step includes it.
@@ -501,6 +614,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="wall-clock budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the widened rows (Nystrom, Stieltjes, deterministic backward)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -410,8 +410,8 @@ struct NysKvCfg {
   static constexpr int kQOff = 0;                      // Qt hi tile, then Qt lo tile
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // barriers: q_full, full[slots], empty[slots], s_full[2], p_full[2], pv_done, done
-  static constexpr int kNumBars = 1 + 2 * kSlots + 6;
+  // barriers: q_full, full[slots], empty[slots], s_full[2], p_full[2], pv_done[2], done
+  static constexpr int kNumBars = 1 + 2 * kSlots + 7;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "more shared memory than one CTA may have");
   static constexpr int kThreads = 256;  // softmax warps 0-1, K-sum warps 2-3 and 6-7, producer, MMA
@@ -433,6 +433,10 @@ struct NysKvCfg {
 // The running max is kept lazily: O and l are rescaled (after the previous
 // P V has completed) only when the tile max exceeds the max in use by more
 // than 8 (log2 units), so the weights in use stay below 2^8.
+// P V completions are signalled on pv_done[u % 2]; the softmax warps observe
+// every phase of each in order (O += P_{j-2} V_{j-2} at tile j, already done by
+// then), because a parity wait on a barrier two phases behind would pass at
+// once, and nothing orders the arrivals of two different commits.
 template <int D>
 __global__ void __launch_bounds__(256, 1)
     nys_kv_kernel(const __grid_constant__ CUtensorMap tm_qt, const __grid_constant__ CUtensorMap tm_k,
@@ -453,8 +457,8 @@ __global__ void __launch_bounds__(256, 1)
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + ST + s); };
   auto bar_s = [&](int b) { return bar0 + 8u * (1 + 2 * ST + b); };
   auto bar_p = [&](int b) { return bar0 + 8u * (3 + 2 * ST + b); };
-  auto bar_pv = [&]() { return bar0 + 8u * (5 + 2 * ST); };
-  auto bar_done = [&]() { return bar0 + 8u * (6 + 2 * ST); };
+  auto bar_pv = [&](int b) { return bar0 + 8u * (5 + 2 * ST + b); };
+  auto bar_done = [&]() { return bar0 + 8u * (7 + 2 * ST); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -470,7 +474,8 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(bar_s(b), 1);
       mbar_init(bar_p(b), nw);
     }
-    mbar_init(bar_pv(), 1);
+    mbar_init(bar_pv(0), 1);
+    mbar_init(bar_pv(1), 1);
     mbar_init(bar_done(), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -542,7 +547,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int kk = 0; kk < 8; ++kk)
           mma_ts_w(tO, tS[u & 1] + kk * 8, v_lo, (uint32_t)((kk * 2048) >> 4), kHi, kIdescO,
                    (u > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar_pv());
+        mma_commit(bar_pv(u & 1));
         mma_commit(bar_empty(sv));
         return true;
       };
@@ -674,12 +679,19 @@ __global__ void __launch_bounds__(256, 1)
       float mx = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 128; ++e) mx = fmaxf(mx, x[e]);
+      // O += P_{jj-2} V_{jj-2} (observed in turn; see above)
+      if (jj >= 2) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_inl(bar_pv(jj & 1), (uint32_t)((jj - 2) >> 1) & 1u, wc));
+        if (!ok) break;
+      }
       const bool raise = mx > mu + 8.f;
       if (__any_sync(0xffffffffu, raise)) {
         const float mnew = raise ? mx : mu;
         if (jj > 0) {
           // O += P_{jj-1} V_{jj-1} must have landed before O is rescaled
-          ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_pv(), (uint32_t)(jj - 1) & 1u, wc));
+          ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_pv((jj - 1) & 1),
+                                                     (uint32_t)((jj - 1) >> 1) & 1u, wc));
           if (!ok) break;
           tc_fence_after();
           const float f = ex2_approx(mu - mnew);
@@ -714,8 +726,8 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p(bb));
     }
-    if (ok && n > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_pv(), (uint32_t)(n - 1) & 1u, wc));
+    // every MMA of the CTA, the last P V included, has completed
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_done(), 0, wc));
     if (ok && n > 0) {
       tc_fence_after();
       const size_t prow = ((size_t)bh * p.kv_chunks + chunk) * m + row;
