@@ -83,6 +83,7 @@ def _kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
+NYS_SOURCES = ["nys_kernel.cuh", "ptx.cuh", "nys.cu", "nys_d128.cu", "nys_d64.cu"]
 FWD_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "fwd_launch.cuh", "fwd_d128.cu", "fwd_d64.cu"]
 BWD_SOURCES = ["bwd_kernel.cuh", "ptx.cuh", "bwd_launch.cuh", "bwd.cu", "bwd_d128.cu",
                "bwd_d64.cu"]
@@ -471,7 +472,9 @@ def next_rows(seed):
             "metric": "forward latency", "value": round(ms, 4), "unit": "ms",
             "higher_is_better": False, "launches": 6,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "traffic": None,
+                         "frac": round(gbs / hbm, 4),
+                         "traffic": _recorded_traffic("nystrom_call", name,
+                                                      _kernel_source_hash(NYS_SOURCES)),
                          "algorithmic_bytes": nbytes,
                          "peak_source": "%s copy bandwidth" % hbm_src,
                          "timed_as": "whole attn_nystrom_fwd call (memset + 6 kernels)"}}
