@@ -30,6 +30,7 @@ SIGNATURES = {
                          _I),
     "attn_fwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_stieltjes_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
+    "attn_fwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_nystrom_fwd": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P], _I),
     "attn_bwd_deterministic": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
                                 _P], _I),
@@ -121,6 +122,14 @@ def attn_stieltjes_fwd(q, k, v, o, pole, B, Hq, Hkv, N, D, causal, scale, order,
     return load().attn_stieltjes_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(pole), B, Hq, Hkv,
                                      N, D, int(bool(causal)), float(scale), int(order),
                                      int(newton_steps), _stream_handle(stream))
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D, causal, scale,
+                    stream=None):
+    """Raw call of the packed variable-length forward; returns the status code."""
+    return load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                                  B, Hq, Hkv, total, max_seqlen, D, int(bool(causal)),
+                                  float(scale), _stream_handle(stream))
 
 
 def attn_nystrom_fwd(q, k, v, o, B, Hq, Hkv, N, D, num_landmarks, newton_iters, kappa, scale,
@@ -303,3 +312,27 @@ def nystrom_attn(q, k, v, num_landmarks=64, newton_iters=6, kappa=5.0, scale=Non
     if st != ATTN_OK:
         raise AttnError(st, "attn_nystrom_fwd")
     return o
+
+
+def flash_attn_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, stream=None):
+    """O [total, Hq, D] and LSE [Hq, total] for sequences packed token-major:
+    q [total, Hq, D], k/v [total, Hkv, D] bf16 on CUDA; cu_seqlens an int32 CUDA
+    tensor [B + 1] of sequence offsets; max_seqlen at least the longest one."""
+    import torch
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    _check(q, (total, Hq, D), "q", torch.bfloat16)
+    _check(k, (total, Hkv, D), "k", torch.bfloat16)
+    _check(v, (total, Hkv, D), "v", torch.bfloat16)
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device)
+    st = attn_fwd_varlen(q, k, v, o, lse, cu_seqlens.contiguous(), B, Hq, Hkv, total,
+                         int(max_seqlen), D, causal, scale, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_varlen")
+    return o, lse

@@ -10,6 +10,7 @@
 
 #include "../../include/attn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace attn {
 
@@ -101,6 +102,22 @@ int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bo
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// 3-D map over a packed token-major bf16 [total, H, D] tensor: dims
+// (D, H, total), box (64, 1, 128) -- 128 tokens of one head, 128-byte rows --
+// with 128-byte swizzle, so a tile lands in shared memory exactly as a tile of
+// the dense map does.  Tokens past `total` read as zero.
+int encode_packed_map(CUtensorMap* map, const void* base, int D, int H, int total) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // 3-D map over a contiguous fp32 [BH, rows, D] array: dims (D, rows, BH), box
 // (32, 128, 1) (128-byte rows), 128-byte swizzle.  Used for the dQ reduce-add.
 int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH) {
@@ -165,12 +182,61 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
   p.err = err;
+  p.scale = scale;
+  p.steps = 0;
+  p.cu_seqlens = nullptr;
+  p.total = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
   cudaError_t e = f16 ? ((D == 64) ? launch_fwd_d64_f16(tq, tk, tv, p, c, s)
                                    : launch_fwd_d128_f16(tq, tk, tv, p, c, s))
                       : ((D == 64) ? launch_fwd_d64(tq, tk, tv, p, c, s)
                                    : launch_fwd_d128(tq, tk, tv, p, c, s));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                     int D, int causal, float scale, void* stream) {
+  if (total < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+  int st = validate_shape(B, Hq, Hkv, max_seqlen, D, scale);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || total == 0 || max_seqlen == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  int dev = 0;
+  unsigned int* err = nullptr;
+  st = device_setup(&dev, &err);
+  if (st != ATTN_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if (encode_packed_map(&tq, q, D, Hq, total) != ATTN_OK ||
+      encode_packed_map(&tk, k, D, Hkv, total) != ATTN_OK ||
+      encode_packed_map(&tv, v, D, Hkv, total) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = max_seqlen;
+  p.G = Hq / Hkv;
+  p.num_qblocks = ((max_seqlen + 127) / 128 + 1) / 2;
+  p.zigzag = 0;
+  p.num_kv_tiles = (max_seqlen + 127) / 128;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_timeout_ns();
+  p.err = err;
+  p.scale = scale;
+  p.steps = 0;
+  p.cu_seqlens = cu_seqlens;
+  p.total = total;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool c = causal != 0;
+  cudaError_t e = (D == 64) ? launch_fwd_varlen_d64(tq, tk, tv, p, c, s)
+                            : launch_fwd_varlen_d128(tq, tk, tv, p, c, s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -210,6 +276,8 @@ int stj_entry(const void* q, const void* k, const void* v, void* o, float* pole,
   p.err = err;
   p.scale = scale;
   p.steps = steps;
+  p.cu_seqlens = nullptr;
+  p.total = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = (D == 64) ? launch_stj_d64(tq, tk, tv, p, causal != 0, order, s)
                             : launch_stj_d128(tq, tk, tv, p, causal != 0, order, s);
@@ -228,7 +296,8 @@ int device_status(void* stream) {
       cudaMemsetAsync(err, 0, sizeof(word), s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  return word ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+  if (word & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+  return word ? ATTN_ERR_INVALID_ARG : ATTN_OK;  // kErrSeqlen: bad cu_seqlens / max_seqlen
 }
 
 int set_wait_timeout_ms(int ms) {
@@ -264,6 +333,13 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  const void* dout, void* dq, void* dk, void* dv) {
   return attn::bwd_entry(q, k, v, o, lse, B, Hq, Hkv, N, D, causal, scale, stream, dout, dq, dk,
                          dv, true);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                    int D, int causal, float scale, void* stream) {
+  return attn::fwd_varlen_entry(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D,
+                                causal, scale, stream);
 }
 
 int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, float* pole, int B,

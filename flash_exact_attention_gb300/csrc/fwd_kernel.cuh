@@ -70,12 +70,63 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-template <int D, bool CAUSAL, bool F16>
+// VARLEN: a batch of sequences of different lengths packed token-major,
+// q/o [total, Hq, D], k/v [total, Hkv, D], lse [Hq, total]; sequence b is
+// rows cu_seqlens[b] .. cu_seqlens[b+1]-1.  The grid is that of a batch of
+// max_seqlen-long sequences (p.N = max_seqlen); CTAs past their sequence's
+// end leave at once.  The TMA maps address a head's rows with a stride of
+// H*D elements (box 64 x 1 head x 128 tokens), which lands in shared memory
+// exactly as a dense tile; key rows past the sequence are masked like a
+// ragged tail and query rows past it are not written.
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D>;
   constexpr int ST = Cfg::kStages;
+
+  // ---- work unit: two 128-row query tiles t0 < t1 of one (batch, head).
+  //  * Non-causal: adjacent tiles (2qb, 2qb+1); the CTAs of one head are
+  //    consecutive so that those resident at one time share its K/V in L2.
+  //  * Causal, grid of at least one wave: adjacent tiles, longest blocks of all
+  //    heads first (both tiles are active in almost every step, so the MMAs of
+  //    one overlap the softmax of the other).
+  //  * Causal, grid smaller than one wave (p.zigzag): tiles qb and T-1-qb, so
+  //    every CTA runs T+1 tile steps; the longest CTA no longer carries two
+  //    full-length tiles, which is what bounds a grid that fits in one wave.
+  const int BH = p.B * p.Hq;
+  const bool zz = CAUSAL && p.zigzag;
+  const int qb = (CAUSAL && !zz) ? p.num_qblocks - 1 - (int)blockIdx.x / BH
+                                 : (int)blockIdx.x % p.num_qblocks;
+  const int bh = (CAUSAL && !zz) ? (int)blockIdx.x % BH : (int)blockIdx.x / p.num_qblocks;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int bh_kv = b * p.Hkv + h / p.G;
+  int seq0 = 0, N = p.N;  // first token and length of this CTA's sequence
+  if constexpr (VARLEN) {
+    seq0 = p.cu_seqlens[b];
+    N = p.cu_seqlens[b + 1] - seq0;
+    if (N < 0 || N > p.N) {  // lengths must lie in [0, max_seqlen]
+      if (threadIdx.x == 0) atomicOr(p.err, kErrSeqlen);
+      return;
+    }
+    if (2 * qb * 128 >= N) return;  // past this sequence's end
+  }
+  const int T = VARLEN ? (N + 127) / 128 : p.num_kv_tiles;
+  const int t0 = zz ? qb : 2 * qb;
+  const int t1 = zz ? T - 1 - qb : 2 * qb + 1;
+  const bool has_t1 = zz ? (t1 > t0) : (t1 * 128 < N);
+  const int n0 = CAUSAL ? t0 + 1 : T;
+  const int n1 = has_t1 ? (CAUSAL ? t1 + 1 : T) : 0;
+  const int nkv = max(n0, n1);
+  // TMA coordinates of a 128-row tile: (column, row, plane) of the dense
+  // (D, N, B*H) map, or (column, head, token) of the packed (D, H, total) map
+  auto load_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c, int tile,
+                       int plane, int head) {
+    if constexpr (VARLEN)
+      tma_load_3d(dst, tm, bar, c * 64, head, seq0 + tile * 128);
+    else
+      tma_load_3d(dst, tm, bar, c * 64, tile * 128, plane);
+  };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
@@ -119,30 +170,6 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-
-  // ---- work unit: two 128-row query tiles t0 < t1 of one (batch, head).
-  //  * Non-causal: adjacent tiles (2qb, 2qb+1); the CTAs of one head are
-  //    consecutive so that those resident at one time share its K/V in L2.
-  //  * Causal, grid of at least one wave: adjacent tiles, longest blocks of all
-  //    heads first (both tiles are active in almost every step, so the MMAs of
-  //    one overlap the softmax of the other).
-  //  * Causal, grid smaller than one wave (p.zigzag): tiles qb and T-1-qb, so
-  //    every CTA runs T+1 tile steps; the longest CTA no longer carries two
-  //    full-length tiles, which is what bounds a grid that fits in one wave.
-  const int T = p.num_kv_tiles;
-  const int BH = p.B * p.Hq;
-  const bool zz = CAUSAL && p.zigzag;
-  const int qb = (CAUSAL && !zz) ? p.num_qblocks - 1 - (int)blockIdx.x / BH
-                                 : (int)blockIdx.x % p.num_qblocks;
-  const int bh = (CAUSAL && !zz) ? (int)blockIdx.x % BH : (int)blockIdx.x / p.num_qblocks;
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int bh_kv = b * p.Hkv + h / p.G;
-  const int t0 = zz ? qb : 2 * qb;
-  const int t1 = zz ? T - 1 - qb : 2 * qb + 1;
-  const bool has_t1 = zz ? (t1 > t0) : (t1 * 128 < p.N);
-  const int n0 = CAUSAL ? t0 + 1 : T;
-  const int n1 = has_t1 ? (CAUSAL ? t1 + 1 : T) : 0;
-  const int nkv = max(n0, n1);
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
 
   if (warp == 8) {
@@ -153,8 +180,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
       for (int t = 0; t < nq; ++t)
         for (int c = 0; c < Cfg::kBoxes; ++c)
-          tma_load_3d(sbase + Cfg::kQOff + t * Cfg::kTileBytes + c * Cfg::kBoxBytes, &tm_q, bar_q(),
-                      c * 64, (t ? t1 : t0) * 128, bh);
+          load_tile(sbase + Cfg::kQOff + t * Cfg::kTileBytes + c * Cfg::kBoxBytes, &tm_q, bar_q(),
+                    c, t ? t1 : t0, bh, h);
       uint32_t it = 0;
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
@@ -166,8 +193,8 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(bar_full(s), Cfg::kTileBytes);
           const CUtensorMap* tm = kv ? &tm_v : &tm_k;
           for (int c = 0; c < Cfg::kBoxes; ++c)
-            tma_load_3d(sbase + Cfg::kRingOff + s * Cfg::kTileBytes + c * Cfg::kBoxBytes, tm,
-                        bar_full(s), c * 64, j * 128, bh_kv);
+            load_tile(sbase + Cfg::kRingOff + s * Cfg::kTileBytes + c * Cfg::kBoxBytes, tm,
+                      bar_full(s), c, j, bh_kv, h / p.G);
         }
       }
       if (!ok) {
@@ -295,8 +322,8 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
       }
       const int kv0 = j * 128;
-      if ((CAUSAL && j == qtile) || kv0 + 128 > p.N) {
-        int lim = p.N - kv0;  // columns >= lim are past the sequence end
+      if ((CAUSAL && j == qtile) || kv0 + 128 > N) {
+        int lim = N - kv0;  // columns >= lim are past the sequence end
         if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // causal: key <= query
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -354,9 +381,11 @@ __global__ void __launch_bounds__(384, 1)
     if (ok && n_t > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const bool live = grow < p.N;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                             ((size_t)bh * p.N + (size_t)(live ? grow : 0)) * D);
+      const bool live = grow < N;
+      // row grow of the output: dense [B*Hq, N, D], or packed [total, Hq, D]
+      const size_t orow_idx = VARLEN ? ((size_t)(seq0 + (live ? grow : 0)) * p.Hq + h)
+                                     : ((size_t)bh * p.N + (size_t)(live ? grow : 0));
+      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * D);
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t r[32];
@@ -374,7 +403,9 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (live) p.lse[(size_t)bh * p.N + grow] = (m_used + log2f(l)) * 0.69314718055994530942f;
+      // LSE: dense [B*Hq, N], packed [Hq, total]
+      const size_t lse_idx = VARLEN ? (size_t)h * p.total + seq0 + grow : (size_t)bh * p.N + grow;
+      if (live) p.lse[lse_idx] = (m_used + log2f(l)) * 0.69314718055994530942f;
     }
   }
 

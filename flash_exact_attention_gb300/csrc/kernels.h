@@ -23,6 +23,10 @@ struct FwdParams {
   // the number of Newton steps.
   float scale;
   int steps;
+  // Packed variable-length forward only: sequence b is tokens
+  // cu_seqlens[b] .. cu_seqlens[b+1]-1 of `total`; N above is max_seqlen.
+  const int* cu_seqlens;
+  int total;
 };
 
 // Nystrom attention forward (six kernels; nys_kernel.cuh).  Landmark rows are
@@ -178,6 +182,14 @@ cudaError_t launch_fwd_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk, con
 cudaError_t launch_fwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const FwdParams& p, bool causal,
                                 cudaStream_t stream);
+
+// Packed variable-length forward (bf16), one kernel per call.
+cudaError_t launch_fwd_varlen_d64(const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const FwdParams& p, bool causal,
+                                  cudaStream_t stream);
+cudaError_t launch_fwd_varlen_d128(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const FwdParams& p, bool causal,
+                                   cudaStream_t stream);
 
 // Stieltjes attention forward (order 2 or 4), one kernel per call.
 cudaError_t launch_stj_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -10,6 +10,9 @@ namespace attn {
 // ------------------------------------------------------------------ error flag
 // Bit set in the device error word when a bounded wait runs out.
 constexpr unsigned kErrTimeout = 1u;
+// Bit set when a kernel finds its per-sequence lengths out of range (a
+// cu_seqlens entry decreasing, or a sequence longer than max_seqlen).
+constexpr unsigned kErrSeqlen = 2u;
 
 // Limits of the bounded waits of one CTA.
 struct WaitCtl {

@@ -122,6 +122,29 @@ int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int newton_steps, void* stream);
 
 /*
+ * Forward over a batch of sequences of different lengths, packed without
+ * padding (bf16).  Each sequence b is an independent attention problem over
+ * its own tokens, exactly as attn_fwd computes for one sequence (causal means
+ * key j <= query i within the sequence).  Token-major packed layout:
+ *   q, o : bf16 [total, Hq, D];  k, v : bf16 [total, Hkv, D];
+ *   lse  : fp32 [Hq, total]  (natural log, as attn_fwd)
+ *   cu_seqlens : int32 DEVICE array [B + 1], cu_seqlens[0] = 0,
+ *                nondecreasing, cu_seqlens[B] = total; sequence b is tokens
+ *                cu_seqlens[b] .. cu_seqlens[b+1] - 1.
+ *   max_seqlen : at least the longest sequence (it sizes the grid).
+ * Ragged sequences without padding: FlashAttention for Tesla P100 page, "What
+ * it supports".  D in {64, 128}; Hq a multiple of Hkv; B, total, max_seqlen
+ * >= 0 (any of them 0: ATTN_OK, nothing launched); pointers 16-byte aligned
+ * (cu_seqlens 4-byte).  Empty sequences are allowed.  The lengths live on the
+ * device, so they are checked there: a decreasing entry or a sequence longer
+ * than max_seqlen leaves that sequence's rows unwritten and makes
+ * attn_device_status() return ATTN_ERR_INVALID_ARG.  One kernel launch.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                    int D, int causal, float scale, void* stream);
+
+/*
  * Nystrom attention forward (bf16 in and out).  FlashNystrom page, "Scope":
  *     O = softmax(s Q Kt^T) . pinv(softmax(s Qt Kt^T)) . softmax(s Qt K^T) . V
  * per (batch, query head), s = scale, every softmax over its rows.  Qt and Kt
