@@ -180,7 +180,8 @@ __device__ __forceinline__ void mm_tiles(const float* At, int lda, const float* 
   }
 }
 
-// mp x mp result (mp in {16, 32, 48, 64}) over K steps into C (row stride mp).
+// mp x mp result (mp in {16, 32, 48, 64}) over K steps into C (row stride mp);
+// ends with a __syncthreads.
 __device__ __forceinline__ void mm_sq(int mp, const float* At, int lda, const float* B, int ldb,
                                       int K, float* C) {
   auto st = [&](int i, int j, float v) { C[i * mp + j] = v; };
@@ -188,8 +189,9 @@ __device__ __forceinline__ void mm_sq(int mp, const float* At, int lda, const fl
     case 16: mm_tiles<1, 1>(At, lda, B, ldb, K, 16, 16, st); break;
     case 32: mm_tiles<1, 2>(At, lda, B, ldb, K, 32, 32, st); break;
     case 48: mm_tiles<2, 3>(At, lda, B, ldb, K, 48, 48, st); break;
-    default: mm_tiles<2, 4>(At, lda, B, ldb, K, 64, 64, st); break;
+    default: mm_tiles<4, 4>(At, lda, B, ldb, K, 64, 64, st); break;
   }
+  __syncthreads();
 }
 
 // max over columns of the column |sums| times max over rows of the row |sums|
@@ -264,16 +266,24 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
 
   // Qt from its fp32 copy, Kt from the key-chunk partial sums of its segments
   // (chunk c_first(i) + k, share s of its tiles wrote slot k * shares + s;
-  // slots of no (chunk, share) pair stay zero)
-  const long long chunk_rows = (long long)p.kv_tpc * 128;
+  // slots of no (chunk, share) pair stay zero).  Per landmark first: the
+  // number of slots and 1 / segment length.
+  int* seg_parts = reinterpret_cast<int*>(red);  // red[0..63]
+  float* seg_inv = red + 64;                     // red[64..127]
+  if (t < m) {
+    const long long chunk_rows = (long long)p.kv_tpc * 128;
+    const long long lo = seg_lo(t, p.N, m), hi = seg_lo(t + 1, p.N, m);
+    seg_parts[t] = ((int)((hi - 1) / chunk_rows - lo / chunk_rows) + 1) * (4 / (D / 64));
+    seg_inv[t] = 1.f / (float)(hi - lo);
+  }
+  __syncthreads();
 #pragma unroll 4
   for (int idx = t; idx < D * mp; idx += 512) {
     const int i = idx / D, d = idx % D;
     float qv = 0.f, kv = 0.f;
     if (i < m) {
       qv = p.qt32[((size_t)bh * m + i) * D + d];
-      const long long lo = seg_lo(i, p.N, m), hi = seg_lo(i + 1, p.N, m);
-      const int parts = ((int)((hi - 1) / chunk_rows - lo / chunk_rows) + 1) * (4 / (D / 64));
+      const int parts = seg_parts[i];
       const float* pk = p.kpart + (((size_t)bhk * m + i) * P) * D + d;
       float s0 = 0.f, s1 = 0.f;  // two chains; the unrolled loads go out together
       int k = 0;
@@ -283,13 +293,13 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
         s1 += pk[(size_t)(k + 1) * D];
       }
       if (k < parts) s0 += pk[(size_t)k * D];
-      kv = (s0 + s1) / (float)(hi - lo);
+      kv = (s0 + s1) * seg_inv[i];
     }
     qtT[d * LD + i] = qv;
     ktT[d * LD + i] = kv;
   }
   for (int idx = t; idx < mp * mp; idx += 512) A[idx] = 0.f;
-  __syncthreads();
+  __syncthreads();  // (also: red is free again)
   if (h % p.G == 0) {  // Kt as a bf16 hi/lo pair of mp-row tiles, once per key head
     uint16_t* dk = p.kt16 + (size_t)bhk * 2 * mp * D;
     for (int idx = t; idx < mp * D; idx += 512) {
@@ -346,7 +356,6 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
   if (ridge) {
     const float lambda = norm1_norminf(A, mp, red) / p.kappa;
     mm_sq(mp, A, mp, A, mp, mp, M);  // (A^T)^T = A
-    __syncthreads();
     for (int i = t; i < m; i += 512) M[i * mp + i] += lambda;
     Mtp = M;
     Xtp = X;
@@ -366,9 +375,7 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
   __syncthreads();
   for (int it = 0; it < p.iters; ++it) {
     mm_sq(mp, Mtp, mp, X, mp, mp, T1);  // M X
-    __syncthreads();
     mm_sq(mp, Xtp, mp, T1, mp, mp, T2);  // X M X
-    __syncthreads();
     for (int idx = t; idx < mp * mp; idx += 512) {
       const float x = 2.f * X[idx] - T2[idx];
       X[idx] = x;
@@ -380,7 +387,6 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
   const float* Pt = Xt;
   if (ridge) {
     mm_sq(mp, At, mp, X, mp, mp, T1);
-    __syncthreads();
     Pt = T1;
   }
 
