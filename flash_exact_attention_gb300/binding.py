@@ -272,6 +272,65 @@ def attention(q, k, v, causal=False, scale=None):
     return o
 
 
+_OPS_REGISTERED = False
+
+
+def register_ops():
+    """Registers torch.ops.flash_exact_attention.fwd / .bwd (torch.library
+    custom ops over attn_fwd / attn_bwd, with shape-only fake implementations
+    and the backward as their autograd formula), so that torch.compile can
+    keep a call inside one graph.  Idempotent; returns the op namespace."""
+    global _OPS_REGISTERED
+    import torch
+    if not _OPS_REGISTERED:
+        @torch.library.custom_op("flash_exact_attention::fwd", mutates_args=())
+        def _fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
+                 scale: float) -> tuple[torch.Tensor, torch.Tensor]:
+            return flash_attn(q, k, v, causal=causal, scale=scale)
+
+        @_fwd.register_fake
+        def _(q, k, v, causal, scale):
+            B, Hq, N, _ = q.shape
+            return torch.empty_like(q), q.new_empty((B, Hq, N), dtype=torch.float32)
+
+        @torch.library.custom_op("flash_exact_attention::bwd", mutates_args=())
+        def _bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                 lse: torch.Tensor, dout: torch.Tensor, causal: bool,
+                 scale: float) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+            return flash_attn_bwd(q, k, v, o, lse, dout.contiguous(), causal=causal, scale=scale)
+
+        @_bwd.register_fake
+        def _(q, k, v, o, lse, dout, causal, scale):
+            return torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def _setup(ctx, inputs, output):
+            q, k, v, causal, scale = inputs
+            o, lse = output
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.causal, ctx.scale = causal, scale
+
+        def _backward(ctx, dout, dlse):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = torch.ops.flash_exact_attention.bwd(q, k, v, o, lse, dout, ctx.causal,
+                                                             ctx.scale)
+            return dq, dk, dv, None, None
+
+        _fwd.register_autograd(_backward, setup_context=_setup)
+        _OPS_REGISTERED = True
+    return torch.ops.flash_exact_attention
+
+
+def attention_op(q, k, v, causal=False, scale=None):
+    """attention() through the registered custom ops.  Inside torch.compile,
+    call register_ops() once beforehand (registration itself is not traceable)."""
+    import torch
+    if not _OPS_REGISTERED:
+        register_ops()
+    o, _ = torch.ops.flash_exact_attention.fwd(
+        q, k, v, bool(causal), 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale))
+    return o
+
+
 def stieltjes_attn(q, k, v, causal=False, scale=None, order=4, newton_steps=3, stream=None):
     """Stieltjes attention (FlashStieltjes page): O and the per-row pole for bf16
     CUDA tensors q [B,Hq,N,D], k/v [B,Hkv,N,D]; order 2 or 4, newton_steps Newton

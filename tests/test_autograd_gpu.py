@@ -36,3 +36,24 @@ def test_attention_default_scale_is_inverse_sqrt_d():
     o_default = binding.attention(t["q"], t["k"], t["v"])
     o_given = binding.attention(t["q"], t["k"], t["v"], scale=scale_for(64))
     assert (o_default == o_given).all()
+
+
+def test_custom_op_gradients_and_compiled_graph():
+    """The custom op gives attention()'s O and gradients bit for bit, and a
+    torch.compile'd function around it traces as one graph (fullgraph=True)."""
+    import torch
+    binding.register_ops()  # before tracing: registration is not traceable
+    t = device_inputs(1, 4, 2, 300, 64, 32, with_do=True)
+    q1, k1, v1 = (t[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    q2, k2, v2 = (t[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    o1 = binding.attention(q1, k1, v1, causal=True)
+    (o1.float() * t["do"].float()).sum().backward()
+    f = torch.compile(lambda q, k, v: binding.attention_op(q, k, v, causal=True),
+                      backend="aot_eager", fullgraph=True)
+    o2 = f(q2, k2, v2)
+    (o2.float() * t["do"].float()).sum().backward()
+    assert binding.attn_device_status() == binding.ATTN_OK
+    assert torch.equal(o1, o2)
+    # dQ is summed by reduce-adds in arrival order: equal to rounding, not bitwise
+    for a, b in ((q1.grad, q2.grad), (k1.grad, k2.grad), (v1.grad, v2.grad)):
+        assert (a.float() - b.float()).abs().max().item() <= 1e-2

@@ -92,3 +92,24 @@ def test_nystrom_is_reproducible():
     outs = [binding.nystrom_attn(t["q"], t["k"], t["v"], num_landmarks=64) for _ in range(3)]
     assert binding.attn_device_status() == binding.ATTN_OK
     assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+@pytest.mark.parametrize("shape,m", [((4, 16, 16, 131072, 128), 64), ((1, 4, 4, 2097152, 64), 32)])
+def test_nystrom_full_size_heads_against_oracle(shape, m):
+    """The page's two shapes at their largest N, in the launch configuration
+    the benchmark times (the whole batch in one call); heads are independent,
+    so two of them are checked against the oracle on their own data."""
+    import torch
+    B, Hq, Hkv, N, D = shape
+    g = torch.Generator(device="cuda").manual_seed(17)
+    q, k, v = (torch.randn(B, Hq, N, D, device="cuda", generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    scale = scale_for(D)
+    o = binding.nystrom_attn(q, k, v, num_landmarks=m, newton_iters=6, kappa=5.0, scale=scale)
+    assert binding.attn_device_status() == binding.ATTN_OK
+    for (b, h) in ((0, 0), (B - 1, Hq - 1)):
+        sl = lambda x: x[b:b + 1, h:h + 1].cpu()
+        ref = oracle.nys_fwd(sl(q), sl(k), sl(v), m, 6, 5.0, scale)
+        got = o[b:b + 1, h:h + 1].float().cpu().numpy()
+        rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert rel <= REL_FRO, ((b, h), float(rel))

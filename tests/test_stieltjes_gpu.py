@@ -54,3 +54,20 @@ def test_stieltjes_rejects_unsupported_order():
     t = device_inputs(1, 2, 2, 128, 64, 1)
     with pytest.raises(binding.AttnError):
         binding.stieltjes_attn(t["q"], t["k"], t["v"], order=3)
+
+
+def test_stieltjes_full_size_sampled_rows():
+    """B=2 H=16 N=8192 D=128 (the dense shape the benchmark times), order 4,
+    three Newton steps: sampled rows (tile edges and random) against the oracle."""
+    from gpu_helpers import sample_rows
+    B, H, N, D = 2, 16, 8192, 128
+    scale = scale_for(D)
+    t = device_inputs(B, H, H, N, D, 21)
+    o, pole = binding.stieltjes_attn(t["q"], t["k"], t["v"], order=4, newton_steps=3, scale=scale)
+    assert binding.attn_device_status() == binding.ATTN_OK
+    rows = sample_rows(B, H, N, 200, 5)
+    ro, rp = oracle.stj_fwd_rows(t["q"].cpu(), t["k"].cpu(), t["v"].cpu(), False, scale, 4, 3, rows)
+    go = o.reshape(-1, D)[rows].float().cpu().numpy()
+    gp = pole.reshape(-1)[rows].cpu().numpy()
+    assert np.abs(go - ro).max() <= O_MAX_ABS
+    assert (np.abs(gp - rp) / np.maximum(1.0, np.abs(rp))).max() <= 1e-3
