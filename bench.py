@@ -438,6 +438,8 @@ def next_rows(seed):
         pooling, output pass), K, V and O once;
       - Stieltjes forward, bound by the tensor cores: steps + 2 QK^T sweeps and
         one P.V per tile pair;
+      - the packed variable-length forward and backward on a ragged causal GQA
+        batch;
       - the deterministic backward, bound by the tensor cores (7 MMAs per tile
         pair counted as the 2.5x-forward convention's 5)."""
     import torch
@@ -499,6 +501,50 @@ def next_rows(seed):
                      "unit": "TFLOP/s", "frac": round(tensor / peak_burst, 4), "traffic": None,
                      "algorithmic_flops_per_launch": 2.0 * B * H * N * N * D * 6,
                      "peak_source": "%s bf16 burst" % peak_src}}
+
+    # Ragged batch, packed without padding: causal GQA (Hq 16, Hkv 4, D 128),
+    # 32 sequences of seeded lengths 1..8192 (about 130 k tokens).
+    import numpy as np
+    Hq, Hkv, D = 16, 4, 128
+    lens = np.random.default_rng(seed).integers(1, 8193, size=32)
+    total, ms_max = int(lens.sum()), int(lens.max())
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(total, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(total, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device="cuda")
+    ms = _time_ms(torch, lambda: binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True))
+    st = binding.attn_device_status()
+    if st:
+        raise binding.AttnError(st, "varlen forward")
+    flops = sum(4.0 * Hq * float(n) * float(n) * D / 2 for n in lens)
+    tf = flops / ms / 1e9
+    rows["varlen_causal_gqa_32seq_d128"] = {
+        "workload": "packed ragged batch, causal GQA Hq=16 Hkv=4 D=128, 32 sequences of "
+                    "seeded lengths 1..8192 (%d tokens, longest %d)" % (total, ms_max),
+        "metric": "forward TFLOPS (sum over sequences of 2 Hq n^2 D)", "value": round(tf, 1),
+        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4), "traffic": None,
+                     "peak_source": "%s bf16 burst" % peak_src}}
+    o, lse = binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True)
+    do = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
+    ms = _time_ms(torch, lambda: binding.flash_attn_varlen_bwd(q, k, v, o, lse, do, cu, ms_max,
+                                                               causal=True))
+    st = binding.attn_device_status()
+    if st:
+        raise binding.AttnError(st, "varlen backward")
+    tf = 2.5 * flops / ms / 1e9
+    rows["varlen_bwd_causal_gqa_32seq_d128"] = {
+        "workload": "backward of the same packed ragged batch (%d tokens)" % total,
+        "metric": "backward TFLOPS (2.5x the forward's FLOPs)", "value": round(tf, 1),
+        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4),
+        "launches": 3, "timed_as": "whole attn_bwd_varlen call (memset + 3 kernels)",
+        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4), "traffic": None,
+                     "peak_source": "%s bf16 burst" % peak_src}}
+    del q, k, v, cu, o, lse, do
+    torch.cuda.empty_cache()
 
     # Deterministic backward on the headline shape.
     t = dev_inputs(B, H, H, N, D, with_do=True)
@@ -618,7 +664,8 @@ def main():
                     help="wall-clock budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
-                    help="skip the widened rows (Nystrom, Stieltjes, deterministic backward)")
+                    help="skip the widened rows (Nystrom, Stieltjes, varlen, deterministic "
+                         "backward)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

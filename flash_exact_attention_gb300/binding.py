@@ -31,6 +31,8 @@ SIGNATURES = {
     "attn_fwd_f16": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_stieltjes_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_fwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_bwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
+                         _P], _I),
     "attn_nystrom_fwd": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P], _I),
     "attn_bwd_deterministic": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
                                 _P], _I),
@@ -130,6 +132,15 @@ def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, 
     return load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
                                   B, Hq, Hkv, total, max_seqlen, D, int(bool(causal)),
                                   float(scale), _stream_handle(stream))
+
+
+def attn_bwd_varlen(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D, causal, scale,
+                    stream, dout, dq, dk, dv):
+    """Raw call of the packed variable-length backward; returns the status code."""
+    return load().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                                  B, Hq, Hkv, total, max_seqlen, D, int(bool(causal)),
+                                  float(scale), _stream_handle(stream), _ptr(dout), _ptr(dq),
+                                  _ptr(dk), _ptr(dv))
 
 
 def attn_nystrom_fwd(q, k, v, o, B, Hq, Hkv, N, D, num_landmarks, newton_iters, kappa, scale,
@@ -395,3 +406,72 @@ def flash_attn_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None,
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_varlen")
     return o, lse
+
+
+def flash_attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, causal=False, scale=None,
+                          stream=None):
+    """dQ [total, Hq, D], dK, dV [total, Hkv, D] of sum(dout * O) for the packed
+    batch flash_attn_varlen computed O [total, Hq, D] and LSE [Hq, total] of."""
+    import torch
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    for t, shp, nm in ((q, (total, Hq, D), "q"), (k, (total, Hkv, D), "k"),
+                       (v, (total, Hkv, D), "v"), (o, (total, Hq, D), "o"),
+                       (dout, (total, Hq, D), "dout")):
+        _check(t, shp, nm, torch.bfloat16)
+    if (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
+            or tuple(lse.shape) != (Hq, total)):
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [Hq, total]")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    st = attn_bwd_varlen(q, k, v, o, lse, cu_seqlens.contiguous(), B, Hq, Hkv, total,
+                         int(max_seqlen), D, causal, scale, stream, dout, dq, dk, dv)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+_VARLEN_FUNCTION = None
+
+
+def _varlen_function():
+    """torch.autograd.Function over attn_fwd_varlen / attn_bwd_varlen."""
+    global _VARLEN_FUNCTION
+    if _VARLEN_FUNCTION is None:
+        import torch
+
+        class VarlenAttnFunction(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, cu_seqlens, max_seqlen, causal, scale):
+                o, lse = flash_attn_varlen(q, k, v, cu_seqlens, max_seqlen, causal=causal,
+                                           scale=scale)
+                ctx.save_for_backward(q, k, v, o, lse, cu_seqlens)
+                ctx.max_seqlen, ctx.causal, ctx.scale = max_seqlen, causal, scale
+                ctx.mark_non_differentiable(lse)
+                return o, lse
+
+            @staticmethod
+            def backward(ctx, dout, dlse):
+                q, k, v, o, lse, cu = ctx.saved_tensors
+                dq, dk, dv = flash_attn_varlen_bwd(q, k, v, o, lse, dout.contiguous(), cu,
+                                                   ctx.max_seqlen, causal=ctx.causal,
+                                                   scale=ctx.scale)
+                return dq, dk, dv, None, None, None, None
+
+        _VARLEN_FUNCTION = VarlenAttnFunction
+    return _VARLEN_FUNCTION
+
+
+def attention_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None):
+    """Differentiable attention over a packed batch of sequences of different
+    lengths (layouts of flash_attn_varlen): the forward is attn_fwd_varlen, the
+    gradient attn_bwd_varlen.  Returns O [total, Hq, D]."""
+    o, _ = _varlen_function().apply(q, k, v, cu_seqlens, int(max_seqlen), bool(causal),
+                                    1.0 / math.sqrt(q.shape[-1]) if scale is None else scale)
+    return o

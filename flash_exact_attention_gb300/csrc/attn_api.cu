@@ -105,13 +105,17 @@ int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bo
 // 3-D map over a packed token-major bf16 [total, H, D] tensor: dims
 // (D, H, total), box (64, 1, 128) -- 128 tokens of one head, 128-byte rows --
 // with 128-byte swizzle, so a tile lands in shared memory exactly as a tile of
-// the dense map does.  Tokens past `total` read as zero.
-int encode_packed_map(CUtensorMap* map, const void* base, int D, int H, int total) {
+// the dense map does.  Tokens past `total` read as zero (and are not written
+// by a store or reduce-add).  f32: an fp32 [total, H, D] tensor, box
+// (32, 1, 128) -- the packed dQ accumulator of the variable-length backward.
+int encode_packed_map(CUtensorMap* map, const void* base, int D, int H, int total, bool f32) {
+  const cuuint64_t es = f32 ? 4 : 2;  // element bytes; a box row is 128 bytes either way
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
+  cuuint32_t box[3] = {f32 ? 32u : 64u, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -340,6 +344,14 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     int D, int causal, float scale, void* stream) {
   return attn::fwd_varlen_entry(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D,
                                 causal, scale, stream);
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                    int D, int causal, float scale, void* stream, const void* dout, void* dq,
+                    void* dk, void* dv) {
+  return attn::bwd_varlen_entry(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D,
+                                causal, scale, stream, dout, dq, dk, dv);
 }
 
 int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, float* pole, int B,

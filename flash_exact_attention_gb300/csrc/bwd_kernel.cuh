@@ -95,13 +95,87 @@ struct BwdCfg {
 };
 
 // DQ = false: dK and dV only (the deterministic backward computes dQ in bwd_dq_kernel).
-template <int D, bool CAUSAL, bool F16, bool DQ = true>
+// VARLEN: sequences packed token-major (BwdParams::cu_seqlens); the grid is
+// that of a batch of max_seqlen-long sequences and CTAs whose key tile lies
+// past their sequence's end leave at once.  The TMA maps are the packed
+// (D, H, total) ones (box 64 x 1 head x 128 tokens; the fp32 dQ map 32 x 1 x
+// 128), whose tiles land in shared memory exactly as dense ones.  Key rows
+// past the sequence are masked like a ragged tail; query rows past it have
+// LSE2 = +inf, so their P, dS and dQ rows are zero (their dQ reduce-adds add
+// zeros to the next sequence's rows).  No group split.
+template <int D, bool CAUSAL, bool F16, bool DQ = true, bool VARLEN = false>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
                const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using Cfg = BwdCfg<D>;
+  static_assert(!(VARLEN && !DQ), "the packed backward has no deterministic variant");
+
+  // ---- work unit: (key tile j, batch, kv head).  Non-causal: the key tiles of
+  // one head are consecutive, so the CTAs resident at one time share a few
+  // heads' Q, dO and dQ accumulator in L2, and each starts its query loop at
+  // tile j so that they add into different dQ tiles at any one time.  Causal:
+  // heaviest key tiles (smallest j) first for load balance, in bands of units
+  // when there are many (a working set of a few heads; see BwdParams::band).
+  const int BHkv = p.B * p.Hkv;
+  const int GS = VARLEN ? 1 : p.gsplit;  // CTAs per (key tile, batch, kv head)
+  int j, unit;
+  if (CAUSAL) {
+    // Key tiles in p.jchunks ranges [c T / K, (c+1) T / K), heaviest range
+    // first; inside a range, bands of p.band units; inside a band, key tile j
+    // ascending (the heaviest CTAs of the band first).
+    const int NU = BHkv * GS, T = p.num_kv_tiles, K = p.jchunks;
+    int c = 0;
+    while (c + 1 < K && (int)blockIdx.x >= ((c + 1) * T / K) * NU) ++c;
+    const int ja = c * T / K, w = (c + 1) * T / K - ja;
+    const int r = (int)blockIdx.x - ja * NU;
+    const int per = p.band * w;
+    const int band = r / per;
+    const int u0 = band * p.band;
+    const int ub = min(p.band, NU - u0);
+    const int r2 = r - band * per;
+    j = ja + r2 / ub;
+    unit = u0 + r2 % ub;
+  } else {
+    j = (int)blockIdx.x % p.num_kv_tiles;
+    unit = (int)blockIdx.x / p.num_kv_tiles;
+  }
+  const int bhkv = unit / GS;
+  const int gi = unit % GS;  // which slice of the group's query heads
+  const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
+  int seq0 = 0, N = p.N;  // first token and length of this CTA's sequence
+  if constexpr (VARLEN) {
+    seq0 = p.cu_seqlens[b];
+    N = p.cu_seqlens[b + 1] - seq0;
+    if (seq0 < 0 || N < 0 || N > p.N || seq0 > p.total - N) {  // not a valid sequence
+      if (threadIdx.x == 0) atomicOr(p.err, kErrSeqlen);
+      return;
+    }
+    if (j * 128 >= N) return;  // past this sequence's end
+  }
+  const int T = VARLEN ? (N + 127) / 128 : p.num_kv_tiles;
+  const int Gs = p.G / GS;  // query heads of this CTA
+  const int i0 = CAUSAL ? j : 0;
+  const int n_i = T - i0;
+  const int n_it = Gs * n_i;
+  auto q_head = [&](int it) {  // flat b*Hq + h
+    return b * p.Hq + hkv * p.G + gi * Gs + it / n_i;
+  };
+  auto q_tile = [&](int it) {
+    const int r = it % n_i;
+    return CAUSAL ? i0 + r : (r + j) % T;
+  };
+  // TMA load of the 128 rows from `row` of one (batch, head): (column, row,
+  // plane) of a dense (D, N, B*H) map, or (column, head, token) of a packed
+  // (D, H, total) one.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int col, int row,
+                       int plane, int head) {
+    if constexpr (VARLEN)
+      tma_load_3d(dst, tm, bar, col, head, seq0 + row);
+    else
+      tma_load_3d(dst, tm, bar, col, row, plane);
+  };
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   // The 128-byte swizzle atoms need a 1024-byte aligned base; there is no room
@@ -162,30 +236,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // ---- work unit: (key tile j, batch, kv head).  Non-causal: the key tiles of
-  // one head are consecutive, so the CTAs resident at one time share a few
-  // heads' Q, dO and dQ accumulator in L2, and each starts its query loop at
-  // tile j so that they add into different dQ tiles at any one time.  Causal:
-  // the heaviest key tiles (smallest j) of all heads go first, for load balance.
-  const int T = p.num_kv_tiles;
-  const int BHkv = p.B * p.Hkv;
-  const int GS = p.gsplit;  // CTAs per (key tile, batch, kv head)
-  const int j = CAUSAL ? (int)blockIdx.x / (BHkv * GS) : (int)blockIdx.x % T;
-  const int unit = CAUSAL ? (int)blockIdx.x % (BHkv * GS) : (int)blockIdx.x / T;
-  const int bhkv = unit / GS;
-  const int gi = unit % GS;  // which slice of the group's query heads
-  const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
-  const int Gs = p.G / GS;  // query heads of this CTA
-  const int i0 = CAUSAL ? j : 0;
-  const int n_i = T - i0;
-  const int n_it = Gs * n_i;
-  auto q_head = [&](int it) {  // flat b*Hq + h
-    return b * p.Hq + hkv * p.G + gi * Gs + it / n_i;
-  };
-  auto q_tile = [&](int it) {
-    const int r = it % n_i;
-    return CAUSAL ? i0 + r : (r + j) % T;
-  };
   const WaitCtl wc{p.timeout_ns, p.err, abort_flag};
   // At D=64 dQ has columns of its own, so dP_{it+1} need not wait for dQ_it to
   // be read out; at D=128 the 512 columns are full and dQ reuses dP's.
@@ -199,8 +249,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       mbar_arrive_expect_tx(bar_kv, 2 * Cfg::kTile);
       for (int c = 0; c < Cfg::kBoxes; ++c) {
-        tma_load_3d(sbase + Cfg::kK + c * Cfg::kBox, &tm_k, bar_kv, c * 64, j * 128, bhkv);
-        tma_load_3d(sbase + Cfg::kV + c * Cfg::kBox, &tm_v, bar_kv, c * 64, j * 128, bhkv);
+        load_rows(sbase + Cfg::kK + c * Cfg::kBox, &tm_k, bar_kv, c * 64, j * 128, bhkv, hkv);
+        load_rows(sbase + Cfg::kV + c * Cfg::kBox, &tm_v, bar_kv, c * 64, j * 128, bhkv, hkv);
       }
       auto load_q = [&](int it) {  // Q_i, LSE2_i, Delta_i into stage it&1
         const int s = it & 1;
@@ -208,16 +258,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t qs = sbase + Cfg::kQ0 + s * Cfg::kTile;
         mbar_arrive_expect_tx(bar_q_full(s), Cfg::kTile + 1024);
         for (int c = 0; c < Cfg::kBoxes; ++c)
-          tma_load_3d(qs + c * Cfg::kBox, &tm_q, bar_q_full(s), c * 64, i * 128, bhq);
+          load_rows(qs + c * Cfg::kBox, &tm_q, bar_q_full(s), c * 64, i * 128, bhq, bhq - b * p.Hq);
         const size_t voff = (size_t)bhq * p.Npad + (size_t)i * 128;
         bulk_load(sbase + Cfg::kVec + s * 1024, p.lse2 + voff, 512, bar_q_full(s));
         bulk_load(sbase + Cfg::kVec + s * 1024 + 512, p.delta + voff, 512, bar_q_full(s));
       };
       auto load_do = [&](int it) {
         mbar_arrive_expect_tx(bar_do_full, Cfg::kTile);
+        const int bhq = q_head(it);
         for (int c = 0; c < Cfg::kBoxes; ++c)
-          tma_load_3d(sbase + Cfg::kdO + c * Cfg::kBox, &tm_do, bar_do_full, c * 64,
-                      q_tile(it) * 128, q_head(it));
+          load_rows(sbase + Cfg::kdO + c * Cfg::kBox, &tm_do, bar_do_full, c * 64,
+                    q_tile(it) * 128, bhq, bhq - b * p.Hq);
       };
       load_q(0);
       load_do(0);
@@ -374,7 +425,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader) {
-          tma_reduce_add_3d(&tm_dq, sbase + Cfg::kdQ + slot, cc * 32, qt * 128, qh);
+          if constexpr (VARLEN)
+            tma_reduce_add_3d(&tm_dq, sbase + Cfg::kdQ + slot, cc * 32, qh - b * p.Hq,
+                              seq0 + qt * 128);
+          else
+            tma_reduce_add_3d(&tm_dq, sbase + Cfg::kdQ + slot, cc * 32, qt * 128, qh);
           bulk_commit();
         }
       }
@@ -399,7 +454,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int ch = warp >> 2;  // query half
     const int row = wq * 32 + lane;  // key row
     const int kj = j * 128 + row;
-    const bool key_live = kj < p.N;
+    const bool key_live = kj < N;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float C = p.scale_log2;
     const float2 c2 = make_float2(C, C);
@@ -528,7 +583,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     } else if (ok) {
       // Epilogue: half 0 writes dV, half 1 writes dK (scaled) of this key row.
       tc_fence_after();
-      const size_t orow = ((size_t)bhkv * p.N + (size_t)(key_live ? kj : 0)) * D;
+      const size_t krow = key_live ? (size_t)kj : 0;
+      const size_t orow = (VARLEN ? ((size_t)seq0 + krow) * p.Hkv + hkv
+                                  : (size_t)bhkv * p.N + krow) * D;
       uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(ch ? p.dk : p.dv) + orow);
       const float mul = ch ? p.scale : 1.f;
       const uint32_t src = (ch ? tdK : tdV) + lane_off;
@@ -610,6 +667,51 @@ __global__ void __launch_bounds__(256)
       zk[t] = make_float4(0.f, 0.f, 0.f, 0.f);
       zv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  }
+}
+
+// Packed variable-length batches: Delta and LSE2 of padded row (b*Hq + h, i),
+// i < Npad, from token cu_seqlens[b] + i of o/dout [total, Hq, D] and lse
+// [Hq, total]; rows past the sequence's end (or of a sequence whose offsets
+// are not valid, which the main kernel reports) get LSE2 = +inf, Delta = 0.
+// One warp per padded row.
+template <int D, bool F16>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_varlen(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                          const float* __restrict__ lse, const int* __restrict__ cu_seqlens,
+                          float* __restrict__ lse2, float* __restrict__ delta, long long rows,
+                          int Hq, int Npad, int max_seqlen, int total) {
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const long long bh = r / Npad;
+  const int i = (int)(r % Npad);
+  const int b = (int)(bh / Hq), h = (int)(bh % Hq);
+  const int seq0 = cu_seqlens[b];
+  const int len = cu_seqlens[b + 1] - seq0;
+  const bool valid = seq0 >= 0 && len >= 0 && len <= max_seqlen && seq0 <= total - len;
+  const bool live = valid && i < len;
+  float acc = 0.f;
+  if (live) {
+    constexpr int kPer = D / 32;
+    const size_t base = ((size_t)(seq0 + i) * Hq + h) * D + (size_t)lane * kPer;
+    if (kPer == 2) {
+      const float2 a = unpack2<F16>(*reinterpret_cast<const uint32_t*>(o + base));
+      const float2 g = unpack2<F16>(*reinterpret_cast<const uint32_t*>(dout + base));
+      acc = a.x * g.x + a.y * g.y;
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+      const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
+      const float2 a0 = unpack2<F16>(a.x), a1 = unpack2<F16>(a.y);
+      const float2 g0 = unpack2<F16>(g.x), g1 = unpack2<F16>(g.y);
+      acc = a0.x * g0.x + a0.y * g0.y + a1.x * g1.x + a1.y * g1.y;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  }
+  if (lane == 0) {
+    lse2[r] = live ? lse[(size_t)h * total + seq0 + i] * 1.4426950408889634f : INFINITY;
+    delta[r] = acc;
   }
 }
 

@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(384, 1)
   if constexpr (VARLEN) {
     seq0 = p.cu_seqlens[b];
     N = p.cu_seqlens[b + 1] - seq0;
-    if (N < 0 || N > p.N) {  // lengths must lie in [0, max_seqlen]
+    // lengths must lie in [0, max_seqlen] and sequences inside [0, total)
+    if (seq0 < 0 || N < 0 || N > p.N || seq0 > p.total - N) {
       if (threadIdx.x == 0) atomicOr(p.err, kErrSeqlen);
       return;
     }

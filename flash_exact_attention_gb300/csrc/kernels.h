@@ -96,6 +96,21 @@ struct BwdParams {
   int gsplit;
   float* dk_acc;
   float* dv_acc;
+  // Causal CTA order.  The key tiles are split into `jchunks` ranges run one
+  // after the other (heaviest first); within a range the work units (one
+  // (batch, kv head[, group slice]) each) go in bands of `band`, key tile j
+  // ascending inside a band.  With many units, bands keep the CTAs resident
+  // at one time on the Q, dO and dQ rows of a few heads (L2) instead of all
+  // of them (HBM); the ranges keep the heaviest CTAs of the last band from
+  // starting at the very end.  band = all units, jchunks = 1: plain j order.
+  int band;
+  int jchunks;
+  // Packed variable-length backward only (else nullptr / 0): sequence b is
+  // tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of q/o/dO/dQ [total, Hq, D] and
+  // k/v/dK/dV [total, Hkv, D]; N is max_seqlen, and lse2/delta are
+  // [B*Hq, Npad] with rows past a sequence's end at +inf / 0.
+  const int* cu_seqlens;
+  int total;
 };
 
 // Device pointers of the backward's fp32 scratch.
@@ -106,6 +121,11 @@ struct BwdScratch {
   float* dk_acc;  // only with gsplit > 1
   float* dv_acc;
 };
+
+// Causal CTA order (BwdParams::band, ::jchunks) for `units` work units of
+// `tiles` key tiles each, whose query-side rows (Q, dO bf16 and the fp32 dQ
+// accumulator) take `unit_bytes`.
+void bwd_order(BwdParams* p, long long units, int tiles, double unit_bytes, int sms);
 
 // Bytes of fp32 scratch the backward needs for these sizes.
 size_t bwd_scratch_bytes(int B, int Hq, int N, int D);
@@ -169,6 +189,8 @@ int device_sm_count(int dev);
 int encode_tile_map(CUtensorMap* map, const void* base, int D, int N, int BH, bool f16 = false,
                     int box_rows = 128);
 int encode_f32_rows_map(CUtensorMap* map, const void* base, int D, int rows, int BH);
+int encode_packed_map(CUtensorMap* map, const void* base, int D, int H, int total,
+                      bool f32 = false);
 uint64_t wait_timeout_ns();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -191,6 +213,19 @@ cudaError_t launch_fwd_varlen_d128(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const FwdParams& p, bool causal,
                                    cudaStream_t stream);
 
+// Packed variable-length backward (bf16): preprocess, main kernel, dQ
+// conversion.  tdq is the packed fp32 map of p.dq_acc [total, Hq, D].
+cudaError_t launch_bwd_varlen_d64(const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const CUtensorMap& tdo,
+                                  const CUtensorMap& tdq, const BwdParams& p, const void* o,
+                                  const void* dout, const float* lse, void* dq, bool causal,
+                                  cudaStream_t stream);
+cudaError_t launch_bwd_varlen_d128(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const CUtensorMap& tdo,
+                                   const CUtensorMap& tdq, const BwdParams& p, const void* o,
+                                   const void* dout, const float* lse, void* dq, bool causal,
+                                   cudaStream_t stream);
+
 // Stieltjes attention forward (order 2 or 4), one kernel per call.
 cudaError_t launch_stj_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const FwdParams& p, bool causal, int order, cudaStream_t stream);
@@ -204,5 +239,9 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
               bool det = false);
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
               int Hkv, int N, int D, int causal, float scale, void* stream, bool f16 = false);
+int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const int* cu_seqlens, int B, int Hq, int Hkv, int total,
+                     int max_seqlen, int D, int causal, float scale, void* stream,
+                     const void* dout, void* dq, void* dk, void* dv);
 
 }  // namespace attn

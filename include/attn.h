@@ -136,13 +136,36 @@ int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, flo
  * it supports".  D in {64, 128}; Hq a multiple of Hkv; B, total, max_seqlen
  * >= 0 (any of them 0: ATTN_OK, nothing launched); pointers 16-byte aligned
  * (cu_seqlens 4-byte).  Empty sequences are allowed.  The lengths live on the
- * device, so they are checked there: a decreasing entry or a sequence longer
- * than max_seqlen leaves that sequence's rows unwritten and makes
- * attn_device_status() return ATTN_ERR_INVALID_ARG.  One kernel launch.
+ * device, so they are checked there: a decreasing entry, a sequence longer
+ * than max_seqlen or one reaching past total leaves that sequence's rows
+ * unwritten and makes attn_device_status() return ATTN_ERR_INVALID_ARG.  One
+ * kernel launch.
  */
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                     const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
                     int D, int causal, float scale, void* stream);
+
+/*
+ * Backward of attn_fwd_varlen (bf16): dq, dk, dv of sum(dout * O), each
+ * sequence independently, from the forward's o and lse (the P recomputation
+ * of attn_bwd: FlashAttention for Tesla P100 page, "Documentation").
+ *   q, o, dout, dq : bf16 [total, Hq, D];  k, v, dk, dv : bf16 [total, Hkv, D];
+ *   lse : fp32 [Hq, total] as attn_fwd_varlen wrote it;
+ *   cu_seqlens, max_seqlen, causal, scale : as given to attn_fwd_varlen.
+ * Sizes, alignment and the device-side check of cu_seqlens as for
+ * attn_fwd_varlen (an invalid sequence leaves its dk/dv rows unwritten and
+ * its dq rows zero; attn_device_status() then returns ATTN_ERR_INVALID_ARG).
+ * Tokens outside every sequence (when cu_seqlens[0] > 0 or cu_seqlens[B] <
+ * total) get dq = 0 and unwritten dk/dv.  dQ is summed in fp32 with atomic
+ * reduce-adds, so its last bits vary from run to run.  Scratch: fp32
+ * total*Hq*D (dQ accumulator) + 2*B*Hq*ceil(max_seqlen/128)*128 (LSE2, Delta),
+ * cudaMallocAsync / cudaFreeAsync on `stream`.  A memset and three kernel
+ * launches.
+ */
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                    int D, int causal, float scale, void* stream, const void* dout, void* dq,
+                    void* dk, void* dv);
 
 /*
  * Nystrom attention forward (bf16 in and out).  FlashNystrom page, "Scope":
@@ -163,8 +186,8 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
  * Landmarks, the landmark softmax, W = softmax(s Qt K^T) V and pinv(A) W are
  * fp32; Qt, Kt, P and pinv(A) W enter the tensor cores as bf16.  Scratch of
  * about (B*Hq + B*Hkv) * m * D * 4 * splits + B*Hq*(chunks*m*(D+2)*4 + ...)
- * bytes is taken with cudaMallocAsync / cudaFreeAsync on `stream`.  Five
- * kernel launches.
+ * bytes is taken with cudaMallocAsync / cudaFreeAsync on `stream`.  A memset
+ * and six kernel launches.
  */
 int attn_nystrom_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                      int Hkv, int N, int D, int num_landmarks, int newton_iters, float kappa,
