@@ -1,14 +1,14 @@
-// fwd_launch.cuh -- host-side launch of fwd_kernel<D, CAUSAL, F16> (one grid per call).
+// fwd_launch.cuh -- host-side launch of fwd_kernel (one grid per call).
 #pragma once
 #include "fwd_kernel.cuh"
 
 namespace attn {
 
-template <int D, bool CAUSAL, bool F16, bool VARLEN = false>
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, F16, VARLEN>;
+  auto kern = fwd_kernel<D, CAUSAL, F16, VARLEN, SPLITP>;
   // Attributes are per device; setting them on every call is cheap and keeps
   // multi-device processes correct.
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
