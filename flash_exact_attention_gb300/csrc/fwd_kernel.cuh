@@ -90,12 +90,21 @@ struct FwdCfg {
 // That shortens the latency of one K/V step (what bounds a grid of less than
 // one wave, where every CTA runs T+1 steps) but adds two barrier waits per
 // step, a net loss when the GPU is full.
-template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false>
+//
+// KVSPLIT: one 128-row query tile per CTA, its key range cut in two halves
+// that the two tile slots (TMEM S/O pairs, softmax warpgroups) process side
+// by side -- slot 0 key tiles [0, n/2), slot 1 [n/2, n) -- and merged at the
+// end from each slot's (max, sum, O).  For grids of less than one wave:
+// every step keeps both slots busy and the longest CTA runs about n/2 steps,
+// where pairing two query tiles (zigzag) leaves one slot idle in most steps.
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false,
+          bool KVSPLIT = false>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D>;
   static_assert(!SPLITP || Cfg::kSplitPOk, "split P needs D = 64");
+  static_assert(!KVSPLIT || (!VARLEN && !SPLITP), "KVSPLIT is a mode of the dense kernel");
   constexpr int ST = Cfg::kStages;
 
   // ---- work unit: two 128-row query tiles t0 < t1 of one (batch, head).
@@ -109,9 +118,11 @@ __global__ void __launch_bounds__(384, 1)
   //    full-length tiles, which is what bounds a grid that fits in one wave.
   const int BH = p.B * p.Hq;
   const bool zz = CAUSAL && p.zigzag;
-  const int qb = (CAUSAL && !zz) ? p.num_qblocks - 1 - (int)blockIdx.x / BH
-                                 : (int)blockIdx.x % p.num_qblocks;
-  const int bh = (CAUSAL && !zz) ? (int)blockIdx.x % BH : (int)blockIdx.x / p.num_qblocks;
+  //  * KVSPLIT: qb is the CTA's one query tile, heaviest first when causal.
+  const int nqb = KVSPLIT ? p.num_kv_tiles : p.num_qblocks;
+  const bool lpt = CAUSAL && (KVSPLIT || !zz);
+  const int qb = lpt ? nqb - 1 - (int)blockIdx.x / BH : (int)blockIdx.x % nqb;
+  const int bh = lpt ? (int)blockIdx.x % BH : (int)blockIdx.x / nqb;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / p.G;
   int seq0 = 0, N = p.N;  // first token and length of this CTA's sequence
@@ -126,11 +137,14 @@ __global__ void __launch_bounds__(384, 1)
     if (2 * qb * 128 >= N) return;  // past this sequence's end
   }
   const int T = VARLEN ? (N + 127) / 128 : p.num_kv_tiles;
-  const int t0 = zz ? qb : 2 * qb;
-  const int t1 = zz ? T - 1 - qb : 2 * qb + 1;
-  const bool has_t1 = zz ? (t1 > t0) : (t1 * 128 < N);
-  const int n0 = CAUSAL ? t0 + 1 : T;
-  const int n1 = has_t1 ? (CAUSAL ? t1 + 1 : T) : 0;
+  const int t0 = (KVSPLIT || zz) ? qb : 2 * qb;
+  const int t1 = KVSPLIT ? qb : (zz ? T - 1 - qb : 2 * qb + 1);
+  const bool has_t1 = KVSPLIT || (zz ? (t1 > t0) : (t1 * 128 < N));
+  // KVSPLIT: the query tile's n_all key tiles, slot 1 starting at tile h0
+  const int n_all = CAUSAL ? qb + 1 : T;
+  const int h0 = KVSPLIT ? n_all / 2 : 0;
+  const int n0 = KVSPLIT ? h0 : (CAUSAL ? t0 + 1 : T);
+  const int n1 = KVSPLIT ? n_all - h0 : (has_t1 ? (CAUSAL ? t1 + 1 : T) : 0);
   const int nkv = max(n0, n1);
   // TMA coordinates of a 128-row tile: (column, row, plane) of the dense
   // (D, N, B*H) map, or (column, head, token) of the packed (D, H, total) map
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ TMA producer
     regs_decrease<Cfg::kRegOther>();
     if (lane == 0) {
-      const int nq = has_t1 ? 2 : 1;
+      const int nq = (has_t1 && !KVSPLIT) ? 2 : 1;
       mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
       for (int t = 0; t < nq; ++t)
         for (int c = 0; c < Cfg::kBoxes; ++c)
@@ -205,7 +219,13 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int j = 0; j < nkv && ok; ++j) {
-        for (int kv = 0; kv < 2 && ok; ++kv, ++it) {
+        // Ring entries of step j: K_j, V_j; with KVSPLIT K of slot 0 (while it
+        // is active) and of slot 1, then V of slot 0 and of slot 1.
+        for (int e = 0; e < (KVSPLIT ? 4 : 2) && ok; ++e) {
+          const int kv = KVSPLIT ? (e >> 1) : e;
+          const int slot = e & 1;
+          if (KVSPLIT && slot == 0 && j >= n0) continue;
+          const int tile = (KVSPLIT && slot) ? h0 + j : j;
           const int s = (int)(it % ST);
           const uint32_t ph = (it / ST) & 1u;
           ok = mbar_wait_inl(bar_empty(s), ph ^ 1u, wc);
@@ -214,7 +234,8 @@ __global__ void __launch_bounds__(384, 1)
           const CUtensorMap* tm = kv ? &tm_v : &tm_k;
           for (int c = 0; c < Cfg::kBoxes; ++c)
             load_tile(sbase + Cfg::kRingOff + s * Cfg::kTileBytes + c * Cfg::kBoxBytes, tm,
-                      bar_full(s), c, j, bh_kv, h / p.G);
+                      bar_full(s), c, tile, bh_kv, h / p.G);
+          ++it;
         }
       }
       if (!ok) {
@@ -237,7 +258,9 @@ __global__ void __launch_bounds__(384, 1)
       // Descriptors as an address word per tile plus a K-step offset added inside
       // the MMA's asm (one register per tile; nothing hoisted per K step).
       constexpr uint32_t kHi = sdesc_sw128_hi(1024);
-      const uint32_t q_lo[2] = {sdesc_sw128_lo(q_addr[0], 16), sdesc_sw128_lo(q_addr[1], 16)};
+      // (KVSPLIT: both slots multiply the one Q tile)
+      const uint32_t q_lo[2] = {sdesc_sw128_lo(q_addr[0], 16),
+                                sdesc_sw128_lo(q_addr[KVSPLIT ? 0 : 1], 16)};
       auto koff = [](int kk) {  // K-major: 32-byte steps inside a 64-column box, then a box
         return (uint32_t)(((kk / 4) * Cfg::kBoxBytes + (kk % 4) * 32) >> 4);
       };
@@ -316,7 +339,66 @@ __global__ void __launch_bounds__(384, 1)
         }
         a1_prev = false;  // nothing left for the common tail below
       }
-      for (int j = 0; j < (SPLITP ? 0 : nkv) && ok; ++j) {
+      if constexpr (KVSPLIT) {
+        // Order per step j, consuming the ring entries in the producer's order
+        // K_0(j), K_1(j), V_0(j), V_1(j): S_0(j); O_1 += P_1(j-1) V_1(j-1);
+        // S_1(j); O_0 += P_0(j) V_0(j) -- each softmax gets the duration of
+        // the other slot's two MMAs, as with two query tiles.
+        auto next = [&](int& s, uint32_t& ph) {
+          s = (int)(it % ST);
+          ph = (it / ST) & 1u;
+          ++it;
+        };
+        int svb = 0;
+        uint32_t phvb = 0;
+        for (int j = 0; j < nkv && ok; ++j) {
+          const bool a0 = j < n0;
+          int s;
+          uint32_t ph;
+          if (a0) {
+            next(s, ph);
+            if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
+            tc_fence_after();
+            issue_qk(0, ring(s));
+            mma_commit(bar_s(0));
+            mma_commit(bar_empty(s));
+          }
+          if (j > 0) {
+            if (!(ok = mbar_wait_inl(bar_full(svb), phvb, wc))) break;
+            if (!(ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) break;
+            ++np1;
+            tc_fence_after();
+            issue_pv(1, ring(svb), j - 1 > 0);
+            mma_commit(bar_empty(svb));
+          }
+          next(s, ph);
+          if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
+          tc_fence_after();
+          issue_qk(1, ring(s));
+          mma_commit(bar_s(1));
+          mma_commit(bar_empty(s));
+          if (a0) {
+            next(s, ph);
+            if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
+            if (!(ok = mbar_wait_inl(bar_p(0), np0 & 1u, wc))) break;
+            ++np0;
+            tc_fence_after();
+            issue_pv(0, ring(s), j > 0);
+            mma_commit(bar_empty(s));
+          }
+          next(svb, phvb);  // V_1(j): waited for where it is used
+        }
+        if (ok && nkv > 0) {
+          ok = mbar_wait_inl(bar_full(svb), phvb, wc) && mbar_wait_inl(bar_p(1), np1 & 1u, wc);
+          if (ok) {
+            ++np1;
+            tc_fence_after();
+            issue_pv(1, ring(svb), nkv - 1 > 0);
+            mma_commit(bar_empty(svb));
+          }
+        }
+      }
+      for (int j = 0; j < ((SPLITP || KVSPLIT) ? 0 : nkv) && ok; ++j) {
         const bool a0 = j < n0, a1 = j < n1;
         const int sk = (int)(it % ST);
         const uint32_t phk = (it / ST) & 1u;
@@ -404,8 +486,9 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_sfree(t));
       }
-      const int kv0 = j * 128;
-      if ((CAUSAL && j == qtile) || kv0 + 128 > N) {
+      const int kvt = (KVSPLIT && t) ? h0 + j : j;  // key tile of this step
+      const int kv0 = kvt * 128;
+      if ((CAUSAL && kvt == qtile) || kv0 + 128 > N) {
         int lim = N - kv0;  // columns >= lim are past the sequence end
         if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // causal: key <= query
 #pragma unroll
@@ -474,8 +557,56 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p(t));
     }
-    if (ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), 0, wc));
-    if (ok && n_t > 0) {
+    if constexpr (KVSPLIT) {
+      // Merge the two slots' partial results of the same rows: each thread
+      // publishes its (m, l) through the unused second Q buffer; then
+      // warpgroup t writes output columns [t D/2, (t+1) D/2) and warpgroup 0
+      // the LSE.
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), 0, wc));
+      float* xm = reinterpret_cast<float*>(smem + Cfg::kQOff + Cfg::kTileBytes);
+      xm[(2 * t) * 128 + row] = m_used;
+      xm[(2 * t + 1) * 128 + row] = l;
+      ok = named_bar_and(1, 256, ok);
+      if (ok) {
+        tc_fence_after();
+        const float m0 = xm[row], l0 = xm[128 + row], m1 = xm[256 + row], l1 = xm[384 + row];
+        const float m = n0 > 0 ? fmaxf(m0, m1) : m1;
+        const float a0 = n0 > 0 ? ex2_approx(m0 - m) : 0.f;
+        const float a1 = ex2_approx(m1 - m);
+        const float L = a0 * l0 + a1 * l1;
+        const float s0 = a0 / L, s1 = a1 / L;
+        const bool live = grow < N;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                               ((size_t)bh * p.N + (size_t)(live ? grow : 0)) * D);
+        const uint32_t tO0 = tmem_base + lane_off + 256u, tO1 = tmem_base + lane_off + 384u;
+#pragma unroll
+        for (int c = t * (D / 2); c < (t + 1) * (D / 2); c += 32) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tO1 + c, r1);
+          if (n0 > 0) tmem_ld32(tO0 + c, r0);
+          tmem_ld_wait();
+          float o[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[i] = __uint_as_float(r1[i]) * s1 + (n0 > 0 ? __uint_as_float(r0[i]) * s0 : 0.f);
+          if (live) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack2<F16>(o[8 * v + 0], o[8 * v + 1]);
+              w.y = pack2<F16>(o[8 * v + 2], o[8 * v + 3]);
+              w.z = pack2<F16>(o[8 * v + 4], o[8 * v + 5]);
+              w.w = pack2<F16>(o[8 * v + 6], o[8 * v + 7]);
+              orow[c / 8 + v] = w;
+            }
+          }
+        }
+        if (t == 0 && live)
+          p.lse[(size_t)bh * p.N + grow] = (m + log2f(L)) * 0.69314718055994530942f;
+      }
+    }
+    if (!KVSPLIT && ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), 0, wc));
+    if (!KVSPLIT && ok && n_t > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool live = grow < N;

@@ -4,17 +4,19 @@
 
 namespace attn {
 
-template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false>
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false,
+          bool KVSPLIT = false>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, F16, VARLEN, SPLITP>;
+  auto kern = fwd_kernel<D, CAUSAL, F16, VARLEN, SPLITP, KVSPLIT>;
   // Attributes are per device; setting them on every call is cheap and keeps
   // multi-device processes correct.
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.num_qblocks * (unsigned)p.B * (unsigned)p.Hq;
+  const unsigned per_head = KVSPLIT ? (unsigned)p.num_kv_tiles : (unsigned)p.num_qblocks;
+  const unsigned grid = per_head * (unsigned)p.B * (unsigned)p.Hq;
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
