@@ -181,15 +181,13 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.num_qblocks = ((N + 127) / 128 + 1) / 2;
   // A causal grid that does not fill the GPU once is bounded by its longest
   // CTA; pairing tile t with tile T-1-t shortens it (see fwd_kernel.cuh).
-  p.zigzag = (causal != 0) && (long long)p.num_qblocks * B * Hq < device_sm_count(dev);
   // Less than one wave of tile pairs: one query tile per CTA, its key range
-  // split over the two slots -- when causal (longest CTA about half the
-  // zigzag one) and when one tile per CTA still fits in a wave.
+  // split over the two slots -- when causal (LPT over single tiles of about
+  // half the steps) and when one tile per CTA still fits in a wave.
   {
     const long long tiles = (long long)((N + 127) / 128) * B * Hq;
     const int sms = device_sm_count(dev);
     p.kvsplit = ((long long)p.num_qblocks * B * Hq < sms) && (causal != 0 || tiles <= sms);
-    if (p.kvsplit) p.zigzag = 0;
   }
   p.num_kv_tiles = (N + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -237,7 +235,6 @@ int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float
   p.N = max_seqlen;
   p.G = Hq / Hkv;
   p.num_qblocks = ((max_seqlen + 127) / 128 + 1) / 2;
-  p.zigzag = 0;
   p.kvsplit = 0;
   p.num_kv_tiles = (max_seqlen + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -283,7 +280,6 @@ int stj_entry(const void* q, const void* k, const void* v, void* o, float* pole,
   p.N = N;
   p.G = Hq / Hkv;
   p.num_qblocks = ((N + 127) / 128 + 1) / 2;
-  p.zigzag = 0;
   p.kvsplit = 0;
   p.num_kv_tiles = (N + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -7,8 +7,8 @@ cudaError_t launch_fwd_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
   // Grids of less than one wave: one query tile per CTA with its key range
   // split over the two slots.
   if (p.kvsplit)
-    return causal ? launch_fwd_impl<128, true, false, false, false, true>(tq, tk, tv, p, stream)
-                  : launch_fwd_impl<128, false, false, false, false, true>(tq, tk, tv, p, stream);
+    return causal ? launch_fwd_impl<128, true, false, false, true>(tq, tk, tv, p, stream)
+                  : launch_fwd_impl<128, false, false, false, true>(tq, tk, tv, p, stream);
   return causal ? launch_fwd_impl<128, true, false>(tq, tk, tv, p, stream)
                 : launch_fwd_impl<128, false, false>(tq, tk, tv, p, stream);
 }

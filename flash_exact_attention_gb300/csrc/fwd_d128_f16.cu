@@ -7,8 +7,8 @@ cudaError_t launch_fwd_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk, co
   // Grids of less than one wave: one query tile per CTA with its key range
   // split over the two slots.
   if (p.kvsplit)
-    return causal ? launch_fwd_impl<128, true, true, false, false, true>(tq, tk, tv, p, stream)
-                  : launch_fwd_impl<128, false, true, false, false, true>(tq, tk, tv, p, stream);
+    return causal ? launch_fwd_impl<128, true, true, false, true>(tq, tk, tv, p, stream)
+                  : launch_fwd_impl<128, false, true, false, true>(tq, tk, tv, p, stream);
   return causal ? launch_fwd_impl<128, true, true>(tq, tk, tv, p, stream)
                 : launch_fwd_impl<128, false, true>(tq, tk, tv, p, stream);
 }

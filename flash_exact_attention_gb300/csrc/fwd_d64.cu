@@ -5,12 +5,10 @@ namespace attn {
 cudaError_t launch_fwd_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, bool causal, cudaStream_t stream) {
   // Grids of less than one wave: one query tile per CTA with its key range
-  // split over the two slots; else, for a causal zigzag grid, P in columns
-  // of its own (a shorter K/V step).
+  // split over the two slots.
   if (p.kvsplit)
-    return causal ? launch_fwd_impl<64, true, false, false, false, true>(tq, tk, tv, p, stream)
-                  : launch_fwd_impl<64, false, false, false, false, true>(tq, tk, tv, p, stream);
-  if (causal && p.zigzag) return launch_fwd_impl<64, true, false, false, true>(tq, tk, tv, p, stream);
+    return causal ? launch_fwd_impl<64, true, false, false, true>(tq, tk, tv, p, stream)
+                  : launch_fwd_impl<64, false, false, false, true>(tq, tk, tv, p, stream);
   return causal ? launch_fwd_impl<64, true, false>(tq, tk, tv, p, stream)
                 : launch_fwd_impl<64, false, false>(tq, tk, tv, p, stream);
 }

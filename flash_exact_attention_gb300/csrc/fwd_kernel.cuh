@@ -59,13 +59,8 @@ struct FwdCfg {
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  // Split P (the kernel's SPLITP mode, D = 64 only: D = 128 has no free
-  // TMEM for it) keeps P in TMEM columns of its own (S0 S1 | O0 P0 | O1 P1,
-  // 64 columns each for O and P) instead of over S.
-  static constexpr bool kSplitPOk = (D == 64);
   // barriers: q_full, full[kStages], empty[kStages], s_full[2], p_full[2], o_final
-  // (+ s_free[2], pv_done[2] for split P)
-  static constexpr int kNumBars = 1 + 2 * kStages + 5 + (kSplitPOk ? 4 : 0);
+  static constexpr int kNumBars = 1 + 2 * kStages + 5;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + misc + alignment slack
   static constexpr int kThreads = 384;
   // Register split (per thread): 8 softmax warps, 4 other warps.
@@ -84,45 +79,32 @@ struct FwdCfg {
 // exactly as a dense tile; key rows past the sequence are masked like a
 // ragged tail and query rows past it are not written.
 //
-// SPLITP (D = 64): P goes to TMEM columns of its own instead of over S, and
-// the softmax warps release S as soon as they have loaded it, so S_t(j+1) is
-// computed while softmax_t(j) still runs instead of after O_t += P_t(j) V_j.
-// That shortens the latency of one K/V step (what bounds a grid of less than
-// one wave, where every CTA runs T+1 steps) but adds two barrier waits per
-// step, a net loss when the GPU is full.
-//
 // KVSPLIT: one 128-row query tile per CTA, its key range cut in two halves
 // that the two tile slots (TMEM S/O pairs, softmax warpgroups) process side
 // by side -- slot 0 key tiles [0, n/2), slot 1 [n/2, n) -- and merged at the
 // end from each slot's (max, sum, O).  For grids of less than one wave:
 // every step keeps both slots busy and the longest CTA runs about n/2 steps,
-// where pairing two query tiles (zigzag) leaves one slot idle in most steps.
-template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false,
-          bool KVSPLIT = false>
+// where pairing query tiles t and T-1-t (so that every CTA runs T+1 steps)
+// leaves one slot idle in most steps.
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool KVSPLIT = false>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D>;
-  static_assert(!SPLITP || Cfg::kSplitPOk, "split P needs D = 64");
-  static_assert(!KVSPLIT || (!VARLEN && !SPLITP), "KVSPLIT is a mode of the dense kernel");
+  static_assert(!KVSPLIT || !VARLEN, "KVSPLIT is a mode of the dense kernel");
   constexpr int ST = Cfg::kStages;
 
   // ---- work unit: two 128-row query tiles t0 < t1 of one (batch, head).
   //  * Non-causal: adjacent tiles (2qb, 2qb+1); the CTAs of one head are
   //    consecutive so that those resident at one time share its K/V in L2.
-  //  * Causal, grid of at least one wave: adjacent tiles, longest blocks of all
-  //    heads first (both tiles are active in almost every step, so the MMAs of
-  //    one overlap the softmax of the other).
-  //  * Causal, grid smaller than one wave (p.zigzag): tiles qb and T-1-qb, so
-  //    every CTA runs T+1 tile steps; the longest CTA no longer carries two
-  //    full-length tiles, which is what bounds a grid that fits in one wave.
+  //  * Causal: adjacent tiles, longest blocks of all heads first (both tiles
+  //    are active in almost every step, so the MMAs of one overlap the
+  //    softmax of the other).
+  //  * KVSPLIT: qb is the CTA's one query tile, longest first when causal.
   const int BH = p.B * p.Hq;
-  const bool zz = CAUSAL && p.zigzag;
-  //  * KVSPLIT: qb is the CTA's one query tile, heaviest first when causal.
   const int nqb = KVSPLIT ? p.num_kv_tiles : p.num_qblocks;
-  const bool lpt = CAUSAL && (KVSPLIT || !zz);
-  const int qb = lpt ? nqb - 1 - (int)blockIdx.x / BH : (int)blockIdx.x % nqb;
-  const int bh = lpt ? (int)blockIdx.x % BH : (int)blockIdx.x / nqb;
+  const int qb = CAUSAL ? nqb - 1 - (int)blockIdx.x / BH : (int)blockIdx.x % nqb;
+  const int bh = CAUSAL ? (int)blockIdx.x % BH : (int)blockIdx.x / nqb;
   const int b = bh / p.Hq, h = bh % p.Hq;
   const int bh_kv = b * p.Hkv + h / p.G;
   int seq0 = 0, N = p.N;  // first token and length of this CTA's sequence
@@ -137,9 +119,9 @@ __global__ void __launch_bounds__(384, 1)
     if (2 * qb * 128 >= N) return;  // past this sequence's end
   }
   const int T = VARLEN ? (N + 127) / 128 : p.num_kv_tiles;
-  const int t0 = (KVSPLIT || zz) ? qb : 2 * qb;
-  const int t1 = KVSPLIT ? qb : (zz ? T - 1 - qb : 2 * qb + 1);
-  const bool has_t1 = KVSPLIT || (zz ? (t1 > t0) : (t1 * 128 < N));
+  const int t0 = KVSPLIT ? qb : 2 * qb;
+  const int t1 = KVSPLIT ? qb : 2 * qb + 1;
+  const bool has_t1 = KVSPLIT || t1 * 128 < N;
   // KVSPLIT: the query tile's n_all key tiles, slot 1 starting at tile h0
   const int n_all = CAUSAL ? qb + 1 : T;
   const int h0 = KVSPLIT ? n_all / 2 : 0;
@@ -170,8 +152,6 @@ __global__ void __launch_bounds__(384, 1)
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + ST + s); };
   auto bar_s = [&](int t) { return bar0 + 8u * (1 + 2 * ST + t); };
   auto bar_p = [&](int t) { return bar0 + 8u * (3 + 2 * ST + t); };
-  auto bar_sfree = [&](int t) { return bar0 + 8u * (6 + 2 * ST + t); };  // SPLITP only
-  auto bar_pv = [&](int t) { return bar0 + 8u * (8 + 2 * ST + t); };     // SPLITP only
   auto bar_o = [&]() { return bar0 + 8u * (5 + 2 * ST); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -184,10 +164,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
-      if constexpr (SPLITP) {
-        mbar_init(bar_sfree(t), 4);
-        mbar_init(bar_pv(t), 1);
-      }
       mbar_init(bar_p(t), 4);
     }
     mbar_init(bar_o(), 1);
@@ -282,63 +258,6 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t it = 0, np0 = 0, np1 = 0;
       int sv_prev = 0;
       bool a1_prev = false;
-      if constexpr (SPLITP) {
-        // Order per K/V step j: S_0(j), S_1(j) (each once its softmax warps have
-        // loaded S_t(j-1)), then O_t += P_t(j-1) V_{j-1} for both tiles.
-        const uint32_t tP[2] = {tmem_base + 320, tmem_base + 448};
-        uint32_t ns[2] = {0, 0}, np[2] = {0, 0};
-        bool a0_prev = false;
-        auto issue_s = [&](int t, uint32_t kaddr) -> bool {
-          if (ns[t] > 0 && !mbar_wait_inl(bar_sfree(t), (ns[t] - 1) & 1u, wc)) return false;
-          tc_fence_after();
-          issue_qk(t, kaddr);
-          mma_commit(bar_s(t));
-          ++ns[t];
-          return true;
-        };
-        auto issue_pv_sp = [&](int t, uint32_t vaddr, bool acc) -> bool {
-          if (!mbar_wait_inl(bar_p(t), np[t] & 1u, wc)) return false;
-          ++np[t];
-          tc_fence_after();
-          const uint32_t v_lo = sdesc_sw128_lo(vaddr, Cfg::kBoxBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts_w(tO[t], tP[t] + kk * 8, v_lo, (uint32_t)((kk * 2048) >> 4), kHi, kIdescO,
-                     (acc || kk > 0) ? 1u : 0u);
-          mma_commit(bar_pv(t));
-          return true;
-        };
-        for (int j = 0; j < nkv && ok; ++j) {
-          const bool a0 = j < n0, a1 = j < n1;
-          const int sk = (int)(it % ST);
-          const uint32_t phk = (it / ST) & 1u;
-          ++it;
-          const int sv = (int)(it % ST);
-          ++it;
-          if (!(ok = mbar_wait_inl(bar_full(sk), phk, wc))) break;
-          tc_fence_after();
-          if (a0 && !(ok = issue_s(0, ring(sk)))) break;
-          if (a1 && !(ok = issue_s(1, ring(sk)))) break;
-          mma_commit(bar_empty(sk));
-          if (j > 0) {
-            // V_{j-1} is in its slot: its full barrier's phase was waited below
-            if (a0_prev && !(ok = issue_pv_sp(0, ring(sv_prev), j - 1 > 0))) break;
-            if (a1_prev && !(ok = issue_pv_sp(1, ring(sv_prev), j - 1 > 0))) break;
-            mma_commit(bar_empty(sv_prev));
-          }
-          const uint32_t phv = ((it - 1) / ST) & 1u;
-          if (!(ok = mbar_wait_inl(bar_full(sv), phv, wc))) break;
-          sv_prev = sv;
-          a0_prev = a0;
-          a1_prev = a1;
-        }
-        if (ok && nkv > 0) {
-          if (a0_prev) ok = issue_pv_sp(0, ring(sv_prev), nkv - 1 > 0);
-          if (ok && a1_prev) ok = issue_pv_sp(1, ring(sv_prev), nkv - 1 > 0);
-          mma_commit(bar_empty(sv_prev));
-        }
-        a1_prev = false;  // nothing left for the common tail below
-      }
       if constexpr (KVSPLIT) {
         // Order per step j, consuming the ring entries in the producer's order
         // K_0(j), K_1(j), V_0(j), V_1(j): S_0(j); O_1 += P_1(j-1) V_1(j-1);
@@ -398,7 +317,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      for (int j = 0; j < ((SPLITP || KVSPLIT) ? 0 : nkv) && ok; ++j) {
+      for (int j = 0; j < (KVSPLIT ? 0 : nkv) && ok; ++j) {
         const bool a0 = j < n0, a1 = j < n1;
         const int sk = (int)(it % ST);
         const uint32_t phk = (it / ST) & 1u;
@@ -480,12 +399,6 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
       }
-      if constexpr (SPLITP) {
-        // S_t(j) is in registers: the MMA warp may write S_t(j+1) now
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree(t));
-      }
       const int kvt = (KVSPLIT && t) ? h0 + j : j;  // key tile of this step
       const int kv0 = kvt * 128;
       if ((CAUSAL && kvt == qtile) || kv0 + 128 > N) {
@@ -520,28 +433,14 @@ __global__ void __launch_bounds__(384, 1)
         const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pp);
         pk[c / 2] = pack2<F16>(pp.x, pp.y);
-        if (!SPLITP && c == 62) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        if (c == 62) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       }
-      if constexpr (SPLITP) {
-        // P_t's columns and O_t are free once O_t += P_t(j-1) V_{j-1} has
-        // completed (that barrier's phases are observed one per step, in order)
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_pv(t), (uint32_t)(j - 1) & 1u, wc));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t tP = tmem_base + lane_off + 320u + (uint32_t)(t * 128);
-        tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      } else {
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      }
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 a = __fadd2_rn(a01, a23);
       l += a.x + a.y;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_t is stable here: its last update was committed before S_t(j)
-        // (with SPLITP: it was waited for above).
+        // O_t is stable here: its last update was committed before S_t(j).
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t r[32];

@@ -4,12 +4,11 @@
 
 namespace attn {
 
-template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool SPLITP = false,
-          bool KVSPLIT = false>
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool KVSPLIT = false>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream) {
   using Cfg = FwdCfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, F16, VARLEN, SPLITP, KVSPLIT>;
+  auto kern = fwd_kernel<D, CAUSAL, F16, VARLEN, KVSPLIT>;
   // Attributes are per device; setting them on every call is cheap and keeps
   // multi-device processes correct.
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

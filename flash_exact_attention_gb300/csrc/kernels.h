@@ -14,7 +14,6 @@ struct FwdParams {
   int B, Hq, Hkv, N;
   int G;                // Hq / Hkv
   int num_qblocks;      // ceil(ceil(N / 128) / 2): CTAs per (batch, head)
-  int zigzag;           // causal only: pair query tiles t and T-1-t (see fwd_kernel.cuh)
   int kvsplit;          // one query tile per CTA, key range split over the two slots
   int num_kv_tiles;     // ceil(N / 128)
   float scale_log2;     // scale * log2(e)
