@@ -179,8 +179,6 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.N = N;
   p.G = Hq / Hkv;
   p.num_qblocks = ((N + 127) / 128 + 1) / 2;
-  // A causal grid that does not fill the GPU once is bounded by its longest
-  // CTA; pairing tile t with tile T-1-t shortens it (see fwd_kernel.cuh).
   // Less than one wave of tile pairs: one query tile per CTA, its key range
   // split over the two slots -- when causal (LPT over single tiles of about
   // half the steps) and when one tile per CTA still fits in a wave.

@@ -104,7 +104,8 @@ def test_empty_inputs_launch_nothing():
 @pytest.mark.parametrize("B,H,N,D", [(1, 16, 4096, 64), (2, 16, 3000, 128)])
 def test_causal_grids_of_more_than_one_wave(B, H, N, D):
     """Causal grids that fill the GPU pair adjacent query tiles; smaller ones
-    pair tile t with tile T-1-t.  The other causal tests mostly take the second
-    form, these take the first (>= 152 CTAs)."""
+    give each CTA one query tile with its key range split over the two slots
+    (KVSPLIT).  The other causal tests mostly take the second form, these take
+    the first (>= 152 CTAs)."""
     t = device_inputs(B, H, H, N, D, 21)
     check_fwd_sampled(t, True, scale_for(D), count=512)
