@@ -101,6 +101,21 @@ def test_empty_inputs_launch_nothing():
     assert binding.attn_fwd(0, 0, 0, 0, 0, 1, 2, 2, 0, 64, False, 0.1) == 0
 
 
+@pytest.mark.parametrize("B,H,Hkv,N,D,causal", [
+    (1, 18, 18, 2000, 128, True),   # 144 tile pairs < 152 SMs: KVSPLIT
+    (1, 19, 19, 2000, 128, True),   # 152 tile pairs: adjacent pairs
+    (1, 16, 4, 1000, 64, False),    # 64 pairs, 128 tiles <= 152: KVSPLIT, ragged tail
+    (1, 16, 16, 2000, 64, False),   # 128 pairs but 256 tiles > 152: adjacent pairs
+    (1, 3, 3, 129, 128, True),      # slot 0 of query tile 0 empty, tile 1 split 1 + 1
+])
+def test_grid_modes_at_the_one_wave_boundary(B, H, Hkv, N, D, causal):
+    """Grids on either side of the switch between the two forward schedules
+    (one query tile per CTA with its key range split over the two slots,
+    below one wave of tile pairs; adjacent tile pairs otherwise)."""
+    t = device_inputs(B, H, Hkv, N, D, 23)
+    check_fwd_sampled(t, causal, scale_for(D), count=512)
+
+
 @pytest.mark.parametrize("B,H,N,D", [(1, 16, 4096, 64), (2, 16, 3000, 128)])
 def test_causal_grids_of_more_than_one_wave(B, H, N, D):
     """Causal grids that fill the GPU pair adjacent query tiles; smaller ones
