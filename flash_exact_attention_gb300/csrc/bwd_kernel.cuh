@@ -528,14 +528,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       {
-        // All 64 dP columns in one round trip (one wait instead of four).
-        uint32_t dra[32], drb[32];
-        tmem_ld32(tp, dra);
-        tmem_ld32(tp + 32, drb);
-        tmem_ld_wait();
-        auto dpv = [&](int q) { return __uint_as_float(q < 32 ? dra[q] : drb[q - 32]); };
+        // dP in two 32-column halves (fewer live registers next to the 64 P
+        // values; the dS^T written below only covers columns of the first half).
+        uint32_t dr[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int hf = 0; hf < 2; ++hf) {
+        tmem_ld32(tp + hf * 32, dr);
+        tmem_ld_wait();
+        auto dpv = [&](int q) { return __uint_as_float(dr[q - 32 * hf]); };
+#pragma unroll
+        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
           uint32_t dk[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {
@@ -561,6 +563,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                          "r"(dk[4 * v]), "r"(dk[4 * v + 1]), "r"(dk[4 * v + 2]), "r"(dk[4 * v + 3])
                          : "memory");
           }
+        }
         }
       }
       tmem_st_wait();
