@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(384, 1)
         ++cnt;
         if (!ok) break;
         tc_fence_after();
-        float s[128];
+        float s[128];  // raw q.k; the scale is folded into the uses below
         {
           uint32_t r[4][32];
 #pragma unroll
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]) * scale;
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
         }
         tc_fence_before();
         __syncwarp();
@@ -286,45 +286,62 @@ __global__ void __launch_bounds__(384, 1)
         const int kv0 = j * 128;
         int lim = p.N - kv0;  // keys >= lim get no weight
         if (CAUSAL) lim = min(lim, grow - kv0 + 1);
+        // Only the diagonal tile and the ragged last tile have keys to mask
+        // (a warp-uniform test); the others take the unmasked loops.
+        const bool masked = (CAUSAL && j == qtile) || kv0 + 128 > p.N;
         if (sw == 0) {
           float mx = -INFINITY;
+          if (masked) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mx = c < lim ? fmaxf(mx, s[c]) : mx;
-          m = fmaxf(m, mx);
-        } else if (!last) {
-          float2 fa = make_float2(0.f, 0.f), ga = make_float2(0.f, 0.f);
+            for (int c = 0; c < 128; ++c) mx = c < lim ? fmaxf(mx, s[c]) : mx;
+          } else {
+            float mp[8];
 #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
-            const float r0 = rcp_approx(pole - s[c]), r1 = rcp_approx(pole - s[c + 1]);
-            float q0 = r0 * r0, q1 = r1 * r1;
-            if (ORDER == 4) {
-              q0 *= q0;
-              q1 *= q1;
-            }
-            const float2 w = make_float2(c < lim ? q0 : 0.f, c + 1 < lim ? q1 : 0.f);
-            fa = __fadd2_rn(fa, w);
-            ga = __ffma2_rn(w, make_float2(r0, r1), ga);
+            for (int k = 0; k < 8; ++k) mp[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+            for (int c = 16; c < 128; c += 16)
+#pragma unroll
+              for (int k = 0; k < 8; ++k) mp[k] = fmax3(mp[k], s[c + k], s[c + 8 + k]);
+            mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
           }
-          f += fa.x + fa.y;
-          g += ga.x + ga.y;
+          m = fmaxf(m, mx * scale);  // scale > 0: the max commutes with it
         } else {
-          uint32_t pk[64];
+          // a = pole - scale s in one fused step per pair; w = a^-q; Newton
+          // sweeps sum w and w / a, the last sweep writes w as P.
+          const float2 ns = make_float2(-scale, -scale), pp = make_float2(pole, pole);
+          auto weights = [&](int c, float2& w, float2& r) {
+            const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), ns, pp);
+            r = make_float2(rcp_approx(a.x), rcp_approx(a.y));
+            w = __fmul2_rn(r, r);
+            if (ORDER == 4) w = __fmul2_rn(w, w);
+            if (masked) w = make_float2(c < lim ? w.x : 0.f, c + 1 < lim ? w.y : 0.f);
+          };
+          if (!last) {
+            float2 fa = make_float2(0.f, 0.f), ga = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
-            const float r0 = rcp_approx(pole - s[c]), r1 = rcp_approx(pole - s[c + 1]);
-            float q0 = r0 * r0, q1 = r1 * r1;
-            if (ORDER == 4) {
-              q0 *= q0;
-              q1 *= q1;
+            for (int c = 0; c < 128; c += 2) {
+              float2 w, r;
+              weights(c, w, r);
+              fa = __fadd2_rn(fa, w);
+              ga = __ffma2_rn(w, r, ga);
             }
-            pk[c / 2] = pack_bf16x2(c < lim ? q0 : 0.f, c + 1 < lim ? q1 : 0.f);
+            f += fa.x + fa.y;
+            g += ga.x + ga.y;
+          } else {
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+              float2 w, r;
+              weights(c, w, r);
+              pk[c / 2] = pack_bf16x2(w.x, w.y);
+            }
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p(t));
           }
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_p(t));
         }
       }
       if (!ok) break;
