@@ -213,8 +213,8 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 }
 
 /*
- * Stieltjes attention forward, a second method on the same tiling (SURVEY's
- * next-ranked row).  FlashStieltjes page, "Why touch softmax": weights
+ * Stieltjes attention forward, a second method on the same tiling.
+ * FlashStieltjes page, "Why touch softmax": weights
  * p_j = (lambda - s_j)^-q with the pole lambda above the best score, placed so
  * that the weights add up to 1; "The challenge": subtract the row's largest
  * score, then Newton-Raphson from lambda = 1.1 (three steps by default);
@@ -296,8 +296,8 @@ int oracle_stj_fwd_rows(const double* q, const double* k, const double* v,
 }
 
 /*
- * Nystrom attention forward (SURVEY's third next-ranked row).  FlashNystrom
- * page, "Scope": the factorisation
+ * Nystrom attention forward, a third method.  FlashNystrom page, "Scope":
+ * the factorisation
  *
  *   O = softmax(Q Kt^T) . pinv(softmax(Qt Kt^T)) . softmax(Qt K^T) . V
  *
