@@ -73,6 +73,38 @@ def test_fwd_rejects_bad_arguments_before_any_device_work(args, expected):
     assert st == expected
 
 
+_VARLEN_OK = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, cu=0x6000, B=2, Hq=4,
+                  Hkv=2, total=300, max_seqlen=200, D=64, causal=1, scale=0.125,
+                  do=0x7000, dq=0x8000, dk=0x9000, dv=0xA000)
+
+
+@pytest.mark.parametrize("args,expected", [
+    (dict(D=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=6, Hkv=4), binding.ATTN_ERR_INVALID_ARG),
+    (dict(total=-1), binding.ATTN_ERR_INVALID_ARG),
+    (dict(max_seqlen=-1), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(cu=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(cu=0x6002), binding.ATTN_ERR_INVALID_ARG),   # offsets not 4-byte aligned
+    (dict(dq=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0x5004), binding.ATTN_ERR_INVALID_ARG),  # not 16-byte aligned
+    (dict(B=0), binding.ATTN_OK),                      # nothing to do
+    (dict(total=0), binding.ATTN_OK),
+])
+def test_varlen_entry_points_reject_bad_arguments_before_any_device_work(args, expected):
+    a = dict(_VARLEN_OK, **args)
+    lib = binding.load()
+    st = lib.attn_bwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["B"], a["Hq"],
+                             a["Hkv"], a["total"], a["max_seqlen"], a["D"], a["causal"],
+                             a["scale"], None, a["do"], a["dq"], a["dk"], a["dv"])
+    assert st == expected
+    if "dq" not in args and "do" not in args:  # the forward takes the same checks
+        st = lib.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cu"], a["B"],
+                                 a["Hq"], a["Hkv"], a["total"], a["max_seqlen"], a["D"],
+                                 a["causal"], a["scale"], None)
+        assert st == expected
+
+
 def test_empty_problem_is_ok_without_device():
     lib = binding.load()
     assert lib.attn_fwd(None, None, None, None, None, 0, 4, 2, 128, 64, 1, 0.1, None) == 0
