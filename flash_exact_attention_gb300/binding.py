@@ -33,6 +33,9 @@ SIGNATURES = {
     "attn_fwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "attn_bwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
                          _P], _I),
+    "attn_fwd_varlen_f16": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "attn_bwd_varlen_f16": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P,
+                             _P, _P], _I),
     "attn_nystrom_fwd": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P], _I),
     "attn_bwd_deterministic": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P,
                                 _P], _I),
@@ -141,6 +144,23 @@ def attn_bwd_varlen(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, 
                                   B, Hq, Hkv, total, max_seqlen, D, int(bool(causal)),
                                   float(scale), _stream_handle(stream), _ptr(dout), _ptr(dq),
                                   _ptr(dk), _ptr(dv))
+
+
+def attn_fwd_varlen_f16(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D, causal,
+                        scale, stream=None):
+    """Raw call of the fp16 packed variable-length forward; returns the status code."""
+    return load().attn_fwd_varlen_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _ptr(cu_seqlens), B, Hq, Hkv, total, max_seqlen, D,
+                                      int(bool(causal)), float(scale), _stream_handle(stream))
+
+
+def attn_bwd_varlen_f16(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D, causal,
+                        scale, stream, dout, dq, dk, dv):
+    """Raw call of the fp16 packed variable-length backward; returns the status code."""
+    return load().attn_bwd_varlen_f16(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _ptr(cu_seqlens), B, Hq, Hkv, total, max_seqlen, D,
+                                      int(bool(causal)), float(scale), _stream_handle(stream),
+                                      _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
 
 
 def attn_nystrom_fwd(q, k, v, o, B, Hq, Hkv, N, D, num_landmarks, newton_iters, kappa, scale,
@@ -386,14 +406,14 @@ def nystrom_attn(q, k, v, num_landmarks=64, newton_iters=6, kappa=5.0, scale=Non
 
 def flash_attn_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, stream=None):
     """O [total, Hq, D] and LSE [Hq, total] for sequences packed token-major:
-    q [total, Hq, D], k/v [total, Hkv, D] bf16 on CUDA; cu_seqlens an int32 CUDA
-    tensor [B + 1] of sequence offsets; max_seqlen at least the longest one."""
+    q [total, Hq, D], k/v [total, Hkv, D] bf16 or fp16 on CUDA; cu_seqlens an int32
+    CUDA tensor [B + 1] of sequence offsets; max_seqlen at least the longest one."""
     import torch
     total, Hq, D = q.shape
     Hkv = k.shape[1]
-    _check(q, (total, Hq, D), "q", torch.bfloat16)
-    _check(k, (total, Hkv, D), "k", torch.bfloat16)
-    _check(v, (total, Hkv, D), "v", torch.bfloat16)
+    _check(q, (total, Hq, D), "q")
+    _check(k, (total, Hkv, D), "k", q.dtype)
+    _check(v, (total, Hkv, D), "v", q.dtype)
     if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
         raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
     B = cu_seqlens.numel() - 1
@@ -401,8 +421,9 @@ def flash_attn_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None,
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q)
     lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device)
-    st = attn_fwd_varlen(q, k, v, o, lse, cu_seqlens.contiguous(), B, Hq, Hkv, total,
-                         int(max_seqlen), D, causal, scale, stream)
+    call = attn_fwd_varlen_f16 if q.dtype == torch.float16 else attn_fwd_varlen
+    st = call(q, k, v, o, lse, cu_seqlens.contiguous(), B, Hq, Hkv, total, int(max_seqlen), D,
+              causal, scale, stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_varlen")
     return o, lse
@@ -418,7 +439,7 @@ def flash_attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, causal=
     for t, shp, nm in ((q, (total, Hq, D), "q"), (k, (total, Hkv, D), "k"),
                        (v, (total, Hkv, D), "v"), (o, (total, Hq, D), "o"),
                        (dout, (total, Hq, D), "dout")):
-        _check(t, shp, nm, torch.bfloat16)
+        _check(t, shp, nm, q.dtype)
     if (lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous()
             or tuple(lse.shape) != (Hq, total)):
         raise ValueError("lse must be a contiguous fp32 CUDA tensor [Hq, total]")
@@ -430,8 +451,9 @@ def flash_attn_varlen_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, causal=
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    st = attn_bwd_varlen(q, k, v, o, lse, cu_seqlens.contiguous(), B, Hq, Hkv, total,
-                         int(max_seqlen), D, causal, scale, stream, dout, dq, dk, dv)
+    call = attn_bwd_varlen_f16 if q.dtype == torch.float16 else attn_bwd_varlen
+    st = call(q, k, v, o, lse, cu_seqlens.contiguous(), B, Hq, Hkv, total, int(max_seqlen), D,
+              causal, scale, stream, dout, dq, dk, dv)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd_varlen")
     return dq, dk, dv

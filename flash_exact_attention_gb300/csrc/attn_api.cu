@@ -206,7 +206,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 
 int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float* lse,
                      const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
-                     int D, int causal, float scale, void* stream) {
+                     int D, int causal, float scale, void* stream, bool f16) {
   if (total < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
   int st = validate_shape(B, Hq, Hkv, max_seqlen, D, scale);
   if (st != ATTN_OK) return st;
@@ -244,8 +244,11 @@ int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float
   p.total = total;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
-  cudaError_t e = (D == 64) ? launch_fwd_varlen_d64(tq, tk, tv, p, c, s)
-                            : launch_fwd_varlen_d128(tq, tk, tv, p, c, s);
+  // (the packed maps only copy 16-bit elements: the same for bf16 and fp16)
+  cudaError_t e = f16 ? ((D == 64) ? launch_fwd_varlen_d64_f16(tq, tk, tv, p, c, s)
+                                   : launch_fwd_varlen_d128_f16(tq, tk, tv, p, c, s))
+                      : ((D == 64) ? launch_fwd_varlen_d64(tq, tk, tv, p, c, s)
+                                   : launch_fwd_varlen_d128(tq, tk, tv, p, c, s));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -357,6 +360,21 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     void* dk, void* dv) {
   return attn::bwd_varlen_entry(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D,
                                 causal, scale, stream, dout, dq, dk, dv);
+}
+
+int attn_fwd_varlen_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                        int D, int causal, float scale, void* stream) {
+  return attn::fwd_varlen_entry(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D,
+                                causal, scale, stream, true);
+}
+
+int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const int* cu_seqlens, int B, int Hq, int Hkv,
+                        int total, int max_seqlen, int D, int causal, float scale, void* stream,
+                        const void* dout, void* dq, void* dk, void* dv) {
+  return attn::bwd_varlen_entry(q, k, v, o, lse, cu_seqlens, B, Hq, Hkv, total, max_seqlen, D,
+                                causal, scale, stream, dout, dq, dk, dv, true);
 }
 
 int attn_stieltjes_fwd(const void* q, const void* k, const void* v, void* o, float* pole, int B,

@@ -167,7 +167,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
 int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const int* cu_seqlens, int B, int Hq, int Hkv, int total,
                      int max_seqlen, int D, int causal, float scale, void* stream,
-                     const void* dout, void* dq, void* dk, void* dv) {
+                     const void* dout, void* dq, void* dk, void* dv, bool f16) {
   if (total < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
   int st = validate_shape(B, Hq, Hkv, max_seqlen, D, scale);
   if (st != ATTN_OK) return st;
@@ -230,9 +230,12 @@ int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o,
     return ATTN_ERR_CUDA;
   }
   const bool c = causal != 0;
-  cudaError_t e = (D == 64)
-      ? launch_bwd_varlen_d64(tq, tk, tv, tdo, tdq, p, o, dout, lse, dq, c, s)
-      : launch_bwd_varlen_d128(tq, tk, tv, tdo, tdq, p, o, dout, lse, dq, c, s);
+  // (the packed maps only copy 16-bit elements: the same for bf16 and fp16)
+  cudaError_t e =
+      f16 ? ((D == 64) ? launch_bwd_varlen_d64_f16(tq, tk, tv, tdo, tdq, p, o, dout, lse, dq, c, s)
+                       : launch_bwd_varlen_d128_f16(tq, tk, tv, tdo, tdq, p, o, dout, lse, dq, c, s))
+          : ((D == 64) ? launch_bwd_varlen_d64(tq, tk, tv, tdo, tdq, p, o, dout, lse, dq, c, s)
+                       : launch_bwd_varlen_d128(tq, tk, tv, tdo, tdq, p, o, dout, lse, dq, c, s));
   st = e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == ATTN_OK) st = ATTN_ERR_CUDA;
   return st;

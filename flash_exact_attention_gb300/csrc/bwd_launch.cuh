@@ -66,7 +66,7 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
 // Packed variable-length backward: LSE2/Delta into padded rows, the main
 // kernel (dQ partials reduce-added into the packed fp32 accumulator p.dq_acc,
 // zeroed here), then dQ = scale * dQacc.  p.N is max_seqlen.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool F16 = false>
 cudaError_t launch_bwd_varlen_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const CUtensorMap& tdo,
                                    const CUtensorMap& tdq, const BwdParams& p, const void* o,
@@ -77,12 +77,12 @@ cudaError_t launch_bwd_varlen_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, (size_t)qrows * D * 4, stream);
   if (e != cudaSuccess) return e;
   const long long prow = (long long)p.B * p.Hq * p.Npad;
-  bwd_preprocess_varlen<D, false><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
+  bwd_preprocess_varlen<D, F16><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, p.cu_seqlens,
       const_cast<float*>(p.lse2), const_cast<float*>(p.delta), prow, p.Hq, p.Npad, p.N, p.total);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = bwd_kernel<D, CAUSAL, false, true, true>;
+  auto kern = bwd_kernel<D, CAUSAL, F16, true, true>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)p.num_kv_tiles * (unsigned)(p.B * p.Hkv);
@@ -93,7 +93,7 @@ cudaError_t launch_bwd_varlen_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   // dQacc and dq have the same packed row order: one "row" of length 1 per
   // (token, head).
   const long long groups = qrows * (D / 8);
-  bwd_postprocess<D, false><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
+  bwd_postprocess<D, F16><<<(unsigned)((groups + 255) / 256), 256, 0, stream>>>(
       p.dq_acc, static_cast<uint16_t*>(dq), qrows, 1, 1, p.scale);
   return cudaGetLastError();
 }

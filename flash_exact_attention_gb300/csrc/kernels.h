@@ -213,7 +213,15 @@ cudaError_t launch_fwd_varlen_d128(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const FwdParams& p, bool causal,
                                    cudaStream_t stream);
 
-// Packed variable-length backward (bf16): preprocess, main kernel, dQ
+// fp16 versions of the packed variable-length forward.
+cudaError_t launch_fwd_varlen_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, const FwdParams& p, bool causal,
+                                      cudaStream_t stream);
+cudaError_t launch_fwd_varlen_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
+                                       const CUtensorMap& tv, const FwdParams& p, bool causal,
+                                       cudaStream_t stream);
+
+// Packed variable-length backward (bf16; _f16: fp16): preprocess, main kernel, dQ
 // conversion.  tdq is the packed fp32 map of p.dq_acc [total, Hq, D].
 cudaError_t launch_bwd_varlen_d64(const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, const CUtensorMap& tdo,
@@ -225,6 +233,16 @@ cudaError_t launch_bwd_varlen_d128(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tdq, const BwdParams& p, const void* o,
                                    const void* dout, const float* lse, void* dq, bool causal,
                                    cudaStream_t stream);
+cudaError_t launch_bwd_varlen_d64_f16(const CUtensorMap& tq, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, const CUtensorMap& tdo,
+                                      const CUtensorMap& tdq, const BwdParams& p, const void* o,
+                                      const void* dout, const float* lse, void* dq, bool causal,
+                                      cudaStream_t stream);
+cudaError_t launch_bwd_varlen_d128_f16(const CUtensorMap& tq, const CUtensorMap& tk,
+                                       const CUtensorMap& tv, const CUtensorMap& tdo,
+                                       const CUtensorMap& tdq, const BwdParams& p, const void* o,
+                                       const void* dout, const float* lse, void* dq, bool causal,
+                                       cudaStream_t stream);
 
 // Stieltjes attention forward (order 2 or 4), one kernel per call.
 cudaError_t launch_stj_d64(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -242,6 +260,9 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 int bwd_varlen_entry(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const int* cu_seqlens, int B, int Hq, int Hkv, int total,
                      int max_seqlen, int D, int causal, float scale, void* stream,
-                     const void* dout, void* dq, void* dk, void* dv);
+                     const void* dout, void* dq, void* dk, void* dv, bool f16 = false);
+int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                     int D, int causal, float scale, void* stream, bool f16 = false);
 
 }  // namespace attn

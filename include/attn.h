@@ -168,6 +168,20 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     void* dk, void* dv);
 
 /*
+ * attn_fwd_varlen / attn_bwd_varlen with fp16 tensors (q, k, v, o, dout, dq,
+ * dk, dv fp16; lse fp32): the same arguments, layouts, checks and errors, and
+ * the arithmetic of attn_fwd_f16 / attn_bwd_f16 (P and dS rounded to fp16 for
+ * the tensor cores, fp32 accumulation).
+ */
+int attn_fwd_varlen_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens, int B, int Hq, int Hkv, int total, int max_seqlen,
+                        int D, int causal, float scale, void* stream);
+int attn_bwd_varlen_f16(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const int* cu_seqlens, int B, int Hq, int Hkv,
+                        int total, int max_seqlen, int D, int causal, float scale, void* stream,
+                        const void* dout, void* dq, void* dk, void* dv);
+
+/*
  * Nystrom attention forward (bf16 in and out).  FlashNystrom page, "Scope":
  *     O = softmax(s Q Kt^T) . pinv(softmax(s Qt Kt^T)) . softmax(s Qt K^T) . V
  * per (batch, query head), s = scale, every softmax over its rows.  Qt and Kt
