@@ -124,3 +124,15 @@ def test_causal_grids_of_more_than_one_wave(B, H, N, D):
     the first (>= 152 CTAs)."""
     t = device_inputs(B, H, H, N, D, 21)
     check_fwd_sampled(t, True, scale_for(D), count=512)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,D,causal", [
+    (1, 2, 1, 262144, 128, True),    # rows attending to up to 2^18 keys; GQA
+    (1, 2, 2, 131072, 64, False),
+])
+def test_very_long_sequences_sampled(B, Hq, Hkv, N, D, causal):
+    """Sampled rows (tile edges, the last rows, random ones) of very long
+    sequences against the oracle: 64-bit offsets, thousands of K/V steps
+    per CTA, LSEs of rows that see ~10^5 keys."""
+    t = device_inputs(B, Hq, Hkv, N, D, 77)
+    check_fwd_sampled(t, causal, scale_for(D), count=48, seed=3)
