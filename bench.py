@@ -54,6 +54,10 @@ WORKLOADS = {
                                 "causal MHA, B=1 H=16 N=2000 D=64 (ragged last tile)"),
     "dense_b1_h2_n256_d64": (1, 2, 2, 256, 64, False,
                              "non-causal MHA, B=1 H=2 N=256 D=64"),
+    "dense_b2_h16_n8192_d64": (2, 16, 16, 8192, 64, False,
+                               "dense non-causal MHA, B=2 H=16 N=8192 D=64"),
+    "causal_b2_h16_n8192_d128": (2, 16, 16, 8192, 128, True,
+                                 "causal MHA, B=2 H=16 N=8192 D=128"),
 }
 DEFAULT_WORKLOAD = "dense_b2_h16_n8192_d128"
 
