@@ -5,8 +5,19 @@ in ``include/attn.h``).  This package only builds that library and marshals
 arguments to it; PyTorch supplies device memory and streams.  There is no CPU
 fallback: if the library is missing the calls raise.
 """
-__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_status_string", "attn_device_status",
-           "flash_attn", "flash_attn_bwd", "AttnError"]
+__all__ = [
+    # C entry points (raw pointers or tensors)
+    "attn_fwd", "attn_bwd", "attn_fwd_f16", "attn_bwd_f16", "attn_bwd_deterministic",
+    "attn_bwd_noalloc", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_varlen_f16",
+    "attn_bwd_varlen_f16", "attn_stieltjes_fwd", "attn_nystrom_fwd", "attn_status_string",
+    "attn_device_status", "attn_set_wait_timeout_ms",
+    # tensor-level calls
+    "flash_attn", "flash_attn_bwd", "flash_attn_varlen", "flash_attn_varlen_bwd",
+    "stieltjes_attn", "nystrom_attn",
+    # autograd and custom ops
+    "attention", "attention_varlen", "register_ops", "attention_op",
+    "AttnError",
+]
 
 
 def __getattr__(name):
