@@ -98,40 +98,183 @@ NYS_SOURCES = ["nys_kernel.cuh", "ptx.cuh", "nys.cu", "nys_d128.cu", "nys_d64.cu
 FWD_SOURCES = ["fwd_kernel.cuh", "ptx.cuh", "fwd_launch.cuh", "fwd_d128.cu", "fwd_d64.cu"]
 BWD_SOURCES = ["bwd_kernel.cuh", "ptx.cuh", "bwd_launch.cuh", "bwd.cu", "bwd_d128.cu",
                "bwd_d64.cu"]
+# Sources of each kernel family: a recorded DRAM figure holds only while their
+# hash is unchanged.
+FAMILY_SOURCES = {
+    "fwd_kernel": FWD_SOURCES + ["fwd_varlen_d128.cu", "fwd_varlen_d64.cu"],
+    "bwd_kernel": BWD_SOURCES + ["bwd_varlen_d128.cu", "bwd_varlen_d64.cu", "bwd_det_d128.cu",
+                                 "bwd_det_d64.cu"],
+    "bwd_dq_kernel": ["bwd_dq_kernel.cuh", "ptx.cuh", "bwd_launch.cuh", "bwd_det_d128.cu",
+                      "bwd_det_d64.cu"],
+    "stj_kernel": ["stj_kernel.cuh", "ptx.cuh", "stj_d128.cu", "stj_d64.cu"],
+    "nystrom_call": NYS_SOURCES,
+}
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
+# Kernel instantiations that only one of the widened rows launches (template
+# arguments as ncu prints them, spaces removed): their DRAM figures are
+# recorded under that row's name whatever --workload says.
+NEXT_ROW_KERNELS = {
+    "stj_kernel<128,false,4>": "stieltjes_b2_h16_n8192_d128_q4",
+    "fwd_kernel<128,true,false,true,false>": "varlen_causal_gqa_32seq_d128",
+    "bwd_kernel<128,true,false,true,true>": "varlen_bwd_causal_gqa_32seq_d128",
+    "bwd_kernel<128,false,false,false,false>": "bwd_deterministic_b2_h16_n8192_d128",
+    "bwd_dq_kernel<128,false,false>": "bwd_deterministic_b2_h16_n8192_d128",
+}
 
 
-def _recorded_traffic(kernel, workload, src_hash):
-    """DRAM bytes per launch from profiles/dram_traffic.md, if taken on this source."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
+def _kernel_source_hash(names):
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "flash_exact_attention_gb300", "csrc")
+    for n in sorted(set(names)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic(family, workload, kernel=None):
+    """DRAM bytes per launch of a kernel family on a workload, from
+    profiles/dram_traffic.json, if recorded on the current sources (else None).
+    `kernel` narrows the match to one instantiation ("fwd_kernel<128,...>")."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
-    for line in open(path):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[2] == src_hash:
-            try:
-                return float(cells[3])
-            except ValueError:
-                return None
+    src_hash = _kernel_source_hash(FAMILY_SOURCES[family])
+    with open(TRAFFIC_JSON) as f:
+        rows = json.load(f).get("rows", [])
+    for r in rows:
+        if (r.get("family") == family and r.get("workload") == workload
+                and r.get("source_hash") == src_hash
+                and (kernel is None or r.get("kernel") == kernel)):
+            return float(r["dram_bytes_per_launch"])
     return None
 
 
-class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+def _traffic_or_why(family, workload, second_family=None):
+    """{"traffic": bytes} from the recorded captures (the sum of both kernels
+    when the call has two), or {"traffic": None, "traffic_note": why}."""
+    t = _recorded_traffic(family, workload)
+    if t is not None and second_family is not None:
+        t2 = _recorded_traffic(second_family, workload)
+        t = None if t2 is None else t + t2
+    if t is None:
+        return {"traffic": None,
+                "traffic_note": "no ncu DRAM capture of this call on the current sources"}
+    return {"traffic": t}
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+
+def _ncu_kernel_key(name):
+    """'void attn::fwd_kernel<128, false, ...>(...)' -> ('fwd_kernel',
+    'fwd_kernel<128,false,...>')."""
+    m = re.search(r"attn::(\w+)<([^>]*)>", name)
+    if not m:
+        m2 = re.search(r"attn::(\w+)", name)
+        fam = m2.group(1) if m2 else name.strip()
+        return fam, fam
+    args = m.group(2).replace(" ", "").replace("(bool)0", "false").replace("(bool)1", "true")
+    return m.group(1), "%s<%s>" % (m.group(1), args)
+
+
+def record_traffic(csv_path, workload, command):
+    """Reads an ncu --csv capture holding dram__bytes_read.sum and
+    dram__bytes_write.sum per launch, and records the median bytes per launch of
+    every kernel of the families above in profiles/dram_traffic.json, keyed by
+    (family, instantiation, workload) with the current source hash."""
+    import csv
+    launches = {}
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        mname = row.get("Metric Name", "")
+        if mname not in ("dram__bytes_read.sum", "dram__bytes_write.sum",
+                         "gpu__time_duration.sum"):
+            continue
+        unit = (row.get("Metric Unit") or "").strip().lower()
+        val = float(row["Metric Value"].replace(",", ""))
+        scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "nsecond": 1e-3,
+                 "usecond": 1.0, "msecond": 1e3, "second": 1e6}.get(unit, 1.0)
+        d = launches.setdefault(row["ID"], {"name": row["Kernel Name"]})
+        d[mname] = d.get(mname, 0.0) + val * scale
+    per_kernel = {}
+    for d in launches.values():
+        fam, key = _ncu_kernel_key(d["name"])
+        if fam not in FAMILY_SOURCES or "dram__bytes_read.sum" not in d:
+            continue
+        per_kernel.setdefault((fam, key), []).append(d)
+    data = {"rows": []}
+    if os.path.exists(TRAFFIC_JSON):
+        with open(TRAFFIC_JSON) as f:
+            data = json.load(f)
+    rows = data.setdefault("rows", [])
+    for (fam, key), ds in sorted(per_kernel.items()):
+        wl = NEXT_ROW_KERNELS.get(key, workload)
+        nbytes = statistics.median(x["dram__bytes_read.sum"] + x["dram__bytes_write.sum"]
+                                   for x in ds)
+        rec = {"family": fam, "kernel": key, "workload": wl,
+               "source_hash": _kernel_source_hash(FAMILY_SOURCES[fam]),
+               "dram_bytes_per_launch": round(nbytes), "launches": len(ds),
+               "command": command}
+        if all("gpu__time_duration.sum" in x for x in ds):
+            rec["gpu_time_us_median_under_ncu"] = round(
+                statistics.median(x["gpu__time_duration.sum"] for x in ds), 2)
+        rows[:] = [r for r in rows if not (r.get("family") == fam and r.get("kernel") == key
+                                           and r.get("workload") == wl)]
+        rows.append(rec)
+        print("recorded %s on %s: %.0f bytes per launch (%d launches)" % (key, wl, nbytes,
+                                                                         len(ds)))
+    data["about"] = ("DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, "
+                     "median over the captured launches) written by `python bench.py "
+                     "--record-traffic <ncu csv> --workload <name>`; bench.py uses a row "
+                     "only while the kernel family's source hash is unchanged")
+    rows.sort(key=lambda r: (r["workload"], r["family"], r["kernel"]))
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(data, f, indent=1)
+        f.write("\n")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running.
+
+    A reader thread stamps every sample with the host clock, so that one
+    sampler can summarise several timed windows (``summary(t0, t1)``)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.samples = []  # (host time, sm MHz, max MHz, set of active reasons)
+        self.thread = None
+
+    def _read(self):
+        import datetime
+        for line in self.proc.stdout:
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 10:
+                continue
+            try:
+                sm, smax = float(c[2]), float(c[3])
+            except ValueError:
+                continue
+            # nvidia-smi's own local-time stamp (its output may reach the pipe
+            # in late chunks); the arrival time if it does not parse
+            try:
+                when = datetime.datetime.strptime(c[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                when = time.time()
+            active = {n for n, val in zip(self.REASONS, c[6:10]) if val.lower() == "active"}
+            self.samples.append((when, sm, smax, active))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
         except (OSError, ValueError):
             self.proc = None
         # nvidia-smi's start-up briefly stalls the device; let it pass before timing.
@@ -139,34 +282,29 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
 
-    def summary(self):
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").splitlines():
-            c = [x.strip() for x in line.split(",")]
-            if len(c) < 9:
-                continue
-            try:
-                sm.append(float(c[1]))
-                smax = float(c[2])
-            except ValueError:
-                continue
-            for name, val in zip(names, c[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in [t0, t1] (host time;
+        the whole run when omitted).  Complete only after the sampler has exited."""
+        sel = [x for x in self.samples
+               if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        smax = sel[-1][2] if sel else (self.samples[-1][2] if self.samples else None)
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = set()
+        for x in sel:
+            reasons |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sel)}
 
 
 def max_over_ranks(values, dist=None, device="cpu"):
@@ -403,19 +541,19 @@ def run_native(args):
                  else "fallback 1.9 PFLOP/s")
     tag = "%d,%s" % (D, "causal" if causal else "noncausal")
 
-    def roof(kernel, sources, tflops, flops):
-        h = _kernel_source_hash(sources)
+    def roof(kernel, family, tflops, flops):
+        h = _kernel_source_hash(FAMILY_SOURCES[family])
         return {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak_burst,
                 "unit": "TFLOP/s", "frac": round(tflops / peak_burst, 4),
-                "traffic": _recorded_traffic(kernel, args.workload, h), "kernel": kernel,
+                "traffic": _recorded_traffic(family, args.workload), "kernel": kernel,
                 "peak_source": peak_note, "frac_of_sustained": round(tflops / peak_sust, 4),
                 "algorithmic_flops_per_launch": flops, "source_hash": h}
 
-    roof_fwd = roof("fwd_kernel<%s>" % tag, FWD_SOURCES, fwd_tflops, ff)
+    roof_fwd = roof("fwd_kernel<%s>" % tag, "fwd_kernel", fwd_tflops, ff)
     if has_bwd:
         # The backward call (preprocess + main + postprocess, timed together) is
         # the dominant part of the step; its FLOPs are the main kernel's.
-        roofline = roof("bwd_kernel<%s>" % tag, BWD_SOURCES, bwd_tflops, 2.5 * ff)
+        roofline = roof("bwd_kernel<%s>" % tag, "bwd_kernel", bwd_tflops, 2.5 * ff)
         roofline["timed_as"] = "whole attn_bwd call (3 launches)"
     else:
         roofline = roof_fwd
@@ -424,15 +562,7 @@ def run_native(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic iid N(0,1) bf16 from numpy seed %d (+rank)" % args.seed,
-        "config": {"workload": desc, "name": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv,
-                   "N": N, "D": D, "causal": causal,
-                   "step": "fwd+bwd" if has_bwd else "fwd (backward not built)",
-                   "parallelism": "replicas" if ws == 1 else "dp%d (independent batches)" % ws,
-                   "l2": ("flushed: a 256 MiB buffer written before every timed step (inputs "
-                          "%.0f MiB fit in the 129 MB L2; one pair of events per step)"
-                          % (in_bytes / 2**20)) if scrub_l2 else
-                         ("no flush: per-step inputs %.0f MiB exceed the 129 MB L2"
-                          % (in_bytes / 2**20))},
+        "config": workload_config(args.workload, ws),
         "fwd_tflops": round(fwd_tflops, 1),
         "fwd_pct_of_peak": round(100 * fwd_tflops / peak_burst, 2),
         "bwd_tflops": round(bwd_tflops, 1) if has_bwd else None,
@@ -445,15 +575,175 @@ def run_native(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if rank == 0 and not args.no_configs:
+        result["configs"] = baseline_configs(args.seed, local)
     if rank == 0 and not args.no_next_rows:
         result["next_rows"] = next_rows(args.seed)
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args.workload, has_bwd, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(args.workload, has_bwd, args.cpu_reps)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+# The five configurations the metric is quoted on (name, (B, Hq, Hkv, N, D,
+# causal), what one step runs, description).  Configuration 4 is a sweep of
+# three shapes of 16384 tokens per batch; configuration 2 has a ragged variant.
+BASELINE_CONFIGS = (
+    ("cfg1_b1_h2_n256_d64", (1, 2, 2, 256, 64, False), "fwd",
+     "fwd, non-causal MHA, B=1 H=2 N=256 D=64"),
+    ("cfg2_causal_b1_h16_n2048_d64", (1, 16, 16, 2048, 64, True), "fwd",
+     "fwd, causal MHA, B=1 H=16 N=2048 D=64"),
+    ("cfg2_causal_b1_h16_n2000_d64", (1, 16, 16, 2000, 64, True), "fwd",
+     "fwd, causal MHA, B=1 H=16 N=2000 D=64 (ragged last tile)"),
+    ("cfg3_causal_gqa_b1_hq8_hkv2_n4096_d128", (1, 8, 2, 4096, 128, True), "fwd",
+     "fwd, causal GQA, B=1 Hq=8 Hkv=2 N=4096 D=128"),
+    ("cfg4_b4_h16_n4096_d128", (4, 16, 16, 4096, 128, False), "fwd",
+     "fwd, dense non-causal MHA, B=4 H=16 N=4096 D=128"),
+    ("cfg4_b2_h16_n8192_d128", (2, 16, 16, 8192, 128, False), "fwd",
+     "fwd, dense non-causal MHA, B=2 H=16 N=8192 D=128"),
+    ("cfg4_b1_h16_n16384_d128", (1, 16, 16, 16384, 128, False), "fwd",
+     "fwd, dense non-causal MHA, B=1 H=16 N=16384 D=128"),
+    ("cfg5_causal_b1_h16_n4096_d64", (1, 16, 16, 4096, 64, True), "fwd+bwd",
+     "fwd+bwd training step, causal MHA, B=1 H=16 N=4096 D=64"),
+)
+
+
+def min_fwd_bytes(B, Hq, Hkv, N, D):
+    """Algorithmic forward traffic: Q, K, V read and O written once (16-bit),
+    LSE written once (fp32)."""
+    return 2 * (2 * B * Hq * N * D + 2 * B * Hkv * N * D) + 4 * B * Hq * N
+
+
+def time_calls(torch, stream, fn, scrub, min_calls=20, min_seconds=0.3, warm=3):
+    """Device time of fn() in ms, one pair of CUDA events per call on `stream`.
+    With `scrub` (a buffer larger than L2) the buffer is written before every
+    call, outside its events, so that each call starts from a cold L2.  Calls
+    go on until at least `min_calls` and `min_seconds` of wall time (enough
+    for the clock sampler to see the load).  Returns (times, host t0, host t1)."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    t0 = time.time()
+    while len(times) < min_calls or time.time() - t0 < min_seconds:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min_calls)]
+        for a, b in evs:
+            if scrub is not None:
+                scrub.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        times += [a.elapsed_time(b) for a, b in evs]
+    return times, t0, time.time()
+
+
+def baseline_configs(seed, local):
+    """Every configuration of the metric, each on its own resident inputs,
+    timed after the headline's timed region (CUDA events on the launch
+    stream, L2 scrubbed before every call when the inputs fit in it)."""
+    import torch
+
+    from flash_exact_attention_gb300 import binding
+    from flash_exact_attention_gb300.synth import make_inputs, scale_for, to_torch_bf16
+
+    peak_burst, peak_sust, peak_src = _measured_peaks()
+    hbm, hbm_src = _measured_hbm()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    scrub = torch.empty(256 * 2**20, dtype=torch.uint8, device="cuda")
+    out, windows = {}, {}
+    with ClockSampler(local) as clk:
+        for name, (B, Hq, Hkv, N, D, causal), what, desc in BASELINE_CONFIGS:
+            scale = scale_for(D)
+            with_bwd = what == "fwd+bwd"
+            x = make_inputs(B, Hq, Hkv, N, D, seed=seed, with_do=with_bwd)
+            t = {n: to_torch_bf16(a).to("cuda") for n, a in x.items()}
+            o = torch.empty_like(t["q"])
+            lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+            if with_bwd:
+                dq, dk, dv = (torch.empty_like(t["q"]), torch.empty_like(t["k"]),
+                              torch.empty_like(t["v"]))
+
+            def fwd():
+                st = binding.attn_fwd(t["q"], t["k"], t["v"], o, lse, B, Hq, Hkv, N, D, causal,
+                                      scale, sh)
+                if st:
+                    raise binding.AttnError(st, "attn_fwd " + name)
+
+            def bwd():
+                st = binding.attn_bwd(t["q"], t["k"], t["v"], o, lse, B, Hq, Hkv, N, D, causal,
+                                      scale, sh, t["do"], dq, dk, dv)
+                if st:
+                    raise binding.AttnError(st, "attn_bwd " + name)
+
+            def step():
+                fwd()
+                bwd()
+
+            in_bytes = sum(a.numel() * a.element_size() for a in t.values())
+            cold = in_bytes < L2_BYTES
+            ff = fwd_flops(B, Hq, N, D, causal)
+            e = {"workload": desc, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "D": D,
+                 "causal": causal, "step": what,
+                 "l2": ("scrubbed: a 256 MiB buffer written before every call (inputs %.1f MiB "
+                        "fit in the 129 MB L2)" % (in_bytes / 2**20)) if cold else
+                       ("not scrubbed: inputs %.0f MiB exceed the 129 MB L2"
+                        % (in_bytes / 2**20))}
+            legs = (("step", step, 3.5 * ff), ("fwd", fwd, ff), ("bwd", bwd, 2.5 * ff)) \
+                if with_bwd else (("fwd", fwd, ff),)
+            w0 = None
+            for leg, fn, flops in legs:
+                times, a, b = time_calls(torch, stream, fn, scrub if cold else None)
+                w0 = a if w0 is None else w0
+                ms = statistics.fmean(times)
+                e[leg + "_ms"] = round(ms, 5)
+                e[leg + "_ms_median"] = round(statistics.median(times), 5)
+                e[leg + "_tflops"] = round(flops / (ms * 1e-3) / 1e12, 2)
+                e["calls"] = len(times)
+            st = binding.attn_device_status(sh)
+            if st:
+                raise binding.AttnError(st, name)
+            main = "step" if with_bwd else "fwd"
+            tf = e[main + "_tflops"]
+            e["tflops"] = tf
+            e["pct_of_peak"] = round(100 * tf / peak_burst, 2)
+            if name.startswith("cfg1"):
+                # Four query tiles: a launch/latency-bound call.  Its figure is a
+                # latency and the bandwidth of its minimal traffic, next to the
+                # rate of back-to-back launches (warm L2, launches queued).
+                nbytes = min_fwd_bytes(B, Hq, Hkv, N, D)
+                ms = e["fwd_ms"]
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                b2b, _, _ = time_calls(torch, stream, fwd, None)
+                e["latency_us"] = round(1e3 * ms, 2)
+                e["back_to_back_us_per_call"] = round(1e3 * statistics.fmean(b2b), 2)
+                e["roofline"] = {
+                    "bound": "latency", "achieved": round(gbs, 2), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 5), "algorithmic_bytes": nbytes,
+                    "peak_source": "%s copy bandwidth" % hbm_src,
+                    "note": "4 CTAs on 152 SMs: launch, first loads and the epilogue, not "
+                            "bandwidth or tensor throughput, set the time"}
+            else:
+                e["roofline"] = {"bound": "tensor", "achieved": tf, "peak": peak_burst,
+                                 "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                                 "frac_of_sustained": round(tf / peak_sust, 4),
+                                 "peak_source": "%s bf16 burst" % peak_src,
+                                 "timed_as": "fwd+bwd step (attn_fwd + attn_bwd)" if with_bwd
+                                 else "attn_fwd (one launch)"}
+            windows[name] = (w0, time.time())
+            out[name] = e
+            del t, o, lse
+            if with_bwd:
+                del dq, dk, dv
+            torch.cuda.empty_cache()
+    for name, (a, b) in windows.items():  # every sample has been read by now
+        out[name]["clocks"] = clk.summary(a, b)
+    return out
 
 
 def _time_ms(torch, fn, warm=3, reps=10):
@@ -515,8 +805,7 @@ def next_rows(seed):
             "higher_is_better": False, "launches": 6,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4),
-                         "traffic": _recorded_traffic("nystrom_call", name,
-                                                      _kernel_source_hash(NYS_SOURCES)),
+                         "traffic": _recorded_traffic("nystrom_call", name),
                          "algorithmic_bytes": nbytes,
                          "peak_source": "%s copy bandwidth" % hbm_src,
                          "timed_as": "whole attn_nystrom_fwd call (memset + 6 kernels)"}}
@@ -538,7 +827,8 @@ def next_rows(seed):
         "metric": "attention TFLOPS (4 B H N^2 D per call)", "value": round(att, 1),
         "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
         "roofline": {"bound": "tensor", "achieved": round(tensor, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tensor / peak_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tensor / peak_burst, 4),
+                     **_traffic_or_why("stj_kernel", "stieltjes_b2_h16_n8192_d128_q4"),
                      "algorithmic_flops_per_launch": 2.0 * B * H * N * N * D * 6,
                      "peak_source": "%s bf16 burst" % peak_src}}
 
@@ -565,7 +855,8 @@ def next_rows(seed):
         "metric": "forward TFLOPS (sum over sequences of 2 Hq n^2 D)", "value": round(tf, 1),
         "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                     **_traffic_or_why("fwd_kernel", "varlen_causal_gqa_32seq_d128"),
                      "peak_source": "%s bf16 burst" % peak_src}}
     o, lse = binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True)
     do = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
@@ -581,7 +872,8 @@ def next_rows(seed):
         "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4),
         "launches": 3, "timed_as": "whole attn_bwd_varlen call (memset + 3 kernels)",
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                     **_traffic_or_why("bwd_kernel", "varlen_bwd_causal_gqa_32seq_d128"),
                      "peak_source": "%s bf16 burst" % peak_src}}
     del q, k, v, cu, o, lse, do
     torch.cuda.empty_cache()
@@ -600,7 +892,9 @@ def next_rows(seed):
         "metric": "backward TFLOPS (2.5x forward FLOPs)", "value": round(tf, 1),
         "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 3,
         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                     **_traffic_or_why("bwd_kernel", "bwd_deterministic_b2_h16_n8192_d128",
+                                       "bwd_dq_kernel"),
                      "peak_source": "%s bf16 burst" % peak_src}}
     del t, o, lse
     torch.cuda.empty_cache()
@@ -612,8 +906,17 @@ BWD_LAUNCHES = 3
 STEP_INCLUDES_BWD = True
 
 
-def cpu_baseline(workload, with_bwd, budget_s):
-    """The fp64 oracle, as it stands, on a bounded sample of the same workload."""
+# The oracle's fixed sample of a workload (the same in the CPU baseline of the
+# native arm and in every step of the reference arm): the forward of
+# ORACLE_FWD_ROWS query rows drawn with numpy seed 1, plus the backward of the
+# first (batch, kv-head) group at full N.
+ORACLE_FWD_ROWS = 2048
+
+
+def oracle_sample(workload, with_bwd, inputs=None):
+    """Runs the oracle's fixed sample once; returns (flops, seconds, description).
+    FLOPs follow the metric's convention: 4*keys*D per forward row (keys = the
+    row's allowed keys), 2.5x the forward of the group for its backward."""
     import numpy as np
 
     import oracle
@@ -621,70 +924,95 @@ def cpu_baseline(workload, with_bwd, budget_s):
 
     B, Hq, Hkv, N, D, causal, _ = WORKLOADS[workload]
     scale = scale_for(D)
-    x = make_inputs(B, Hq, Hkv, N, D, seed=0, with_do=with_bwd)
-    q, k, v = (bf16_bits_to_f32(x[n]) for n in ("q", "k", "v"))
-    rng = np.random.default_rng(1)
-    flops = 0.0
+    if inputs is None:
+        x = make_inputs(B, Hq, Hkv, N, D, seed=0, with_do=with_bwd)
+        inputs = {n: bf16_bits_to_f32(a) for n, a in x.items()}
+    q, k, v = inputs["q"], inputs["k"], inputs["v"]
+    rows = np.random.default_rng(1).integers(0, B * Hq * N, size=ORACLE_FWD_ROWS)
+    i = rows % N
+    keys = (i + 1) if causal else np.full_like(i, N)
+    flops = float(np.sum(4.0 * keys * D))
     t0 = time.perf_counter()
-    rows_done = 0
-    # forward on random rows in batches until the time budget is spent
-    fwd_budget = budget_s / (3.5 if with_bwd else 1.0)
-    while time.perf_counter() - t0 < fwd_budget:
-        rows = rng.integers(0, B * Hq * N, size=max(64, oracle.num_threads() * 16))
-        oracle.fwd_rows(q, k, v, causal, scale, rows)
-        i = rows % N
-        keys = (i + 1) if causal else np.full_like(i, N)
-        flops += float(np.sum(4.0 * keys * D))
-        rows_done += rows.size
-    t_fwd = time.perf_counter() - t0
-    sample = "forward of %d random rows" % rows_done
-    t_bwd = 0.0
+    oracle.fwd_rows(q, k, v, causal, scale, rows)
+    desc = "forward of %d seeded rows" % ORACLE_FWD_ROWS
+    G = Hq // Hkv
     if with_bwd:
-        # backward of the first (batch, kv-head) group of the same workload
-        t1 = time.perf_counter()
-        sl = slice(0, Hq // Hkv)
-        qq = q[:1, sl]
-        kk = k[:1, :1]
-        vv = v[:1, :1]
-        dd = bf16_bits_to_f32(x["do"])[:1, sl]
-        oracle.bwd(qq, kk, vv, dd, causal, scale)
-        t_bwd = time.perf_counter() - t1
-        flops += 2.5 * fwd_flops(1, Hq // Hkv, N, D, causal)
-        sample += " + backward of one (batch, kv-head) group (%d query heads)" % (Hq // Hkv)
-    secs = t_fwd + t_bwd
-    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT,
-            "cores": oracle.num_threads(), "kind": "oracle", "sample": sample,
-            "seconds": round(secs, 2), "host_cpus": os.cpu_count()}
+        sl = slice(0, G)
+        oracle.bwd(q[:1, sl], k[:1, :1], v[:1, :1], inputs["do"][:1, sl], causal, scale)
+        flops += 2.5 * fwd_flops(1, G, N, D, causal)
+        desc += " + backward of the (batch 0, kv-head 0) group (%d query head%s, N=%d)" % (
+            G, "s" if G > 1 else "", N)
+    return flops, time.perf_counter() - t0, desc
+
+
+def _oracle_inputs(workload, with_bwd):
+    from flash_exact_attention_gb300.synth import bf16_bits_to_f32, make_inputs
+    B, Hq, Hkv, N, D, _, _ = WORKLOADS[workload]
+    x = make_inputs(B, Hq, Hkv, N, D, seed=0, with_do=with_bwd)
+    return {n: bf16_bits_to_f32(a) for n, a in x.items()}
+
+
+def cpu_baseline(workload, with_bwd, reps=4):
+    """The fp64 oracle, as it stands, on the host cores: its fixed sample of
+    the workload, run `reps` times; the median rate."""
+    import oracle
+    inputs = _oracle_inputs(workload, with_bwd)
+    runs = [oracle_sample(workload, with_bwd, inputs) for _ in range(reps)]
+    rates = [f / sec / 1e12 for f, sec, _ in runs]
+    return {"value": round(statistics.median(rates), 6), "unit": UNIT,
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": runs[0][2] + "; %d runs, median rate" % reps,
+            "sample_flops": runs[0][0],
+            "seconds": round(sum(sec for _, sec, _ in runs), 2), "host_cpus": os.cpu_count()}
+
+
+def workload_config(workload, ws):
+    """The `config` object of the JSON line (the same in both arms)."""
+    B, Hq, Hkv, N, D, causal, desc = WORKLOADS[workload]
+    x_bytes = 2 * (2 * B * Hq * N * D + 2 * B * Hkv * N * D)  # q, k, v, dO (16-bit)
+    scrub = x_bytes < L2_BYTES
+    return {"workload": desc, "name": workload, "B": B, "Hq": Hq, "Hkv": Hkv,
+            "N": N, "D": D, "causal": causal,
+            "step": "fwd+bwd" if STEP_INCLUDES_BWD else "fwd (backward not built)",
+            "parallelism": "replicas" if ws == 1 else "dp%d (independent batches)" % ws,
+            "l2": ("flushed: a 256 MiB buffer written before every timed step (inputs "
+                   "%.0f MiB fit in the 129 MB L2; one pair of events per step)"
+                   % (x_bytes / 2**20)) if scrub else
+                  ("no flush: per-step inputs %.0f MiB exceed the 129 MB L2"
+                   % (x_bytes / 2**20))}
 
 
 def run_reference(args):
+    """The reference arm: the fp64 CPU oracle (there is no other
+    implementation of the pages' method to install), each step its fixed
+    sample of the workload, on the host cores."""
     ws, rank, _ = _dist_env()
     if rank != 0:
         return
     has_bwd = STEP_INCLUDES_BWD
-    B, Hq, Hkv, N, D, causal, desc = WORKLOADS[args.workload]
     import oracle
     oracle.build()
+    inputs = _oracle_inputs(args.workload, has_bwd)
     for _ in range(args.warmup):
-        cpu_baseline(args.workload, has_bwd, 0.2)
-    vals = []
+        oracle_sample(args.workload, has_bwd, inputs)
+    runs = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(args.workload, has_bwd, args.cpu_seconds / max(1, args.steps)))
+        runs.append(oracle_sample(args.workload, has_bwd, inputs))
     wall = time.perf_counter() - t0
-    value = statistics.median(v["value"] for v in vals)
-    cb = dict(vals[-1])
-    cb["value"] = value
+    flops = sum(f for f, _, _ in runs)
+    secs = sum(sec for _, sec, _ in runs)
+    value = round(flops / secs / 1e12, 6)
+    cb = {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": runs[0][2] + " per step", "sample_flops": runs[0][0],
+          "seconds": round(secs, 2), "host_cpus": os.cpu_count()}
     result = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * wall / max(1, args.steps), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic iid N(0,1) bf16 from numpy seed 0",
-        "config": {"workload": desc, "name": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv,
-                   "N": N, "D": D, "causal": causal,
-                   "step": "fwd+bwd" if has_bwd else "fwd",
-                   "note": "the fp64 CPU oracle on a bounded sample of the workload per step"},
+        "data": "synthetic iid N(0,1) bf16 from numpy seed %d (+rank)" % 0,
+        "config": workload_config(args.workload, ws),
         "cpu_baseline": cb,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -700,13 +1028,24 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="wall-clock budget of the oracle CPU baseline")
+    ap.add_argument("--cpu-reps", type=int, default=4,
+                    help="runs of the oracle's fixed sample in the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other configurations of the metric")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the widened rows (Nystrom, Stieltjes, varlen, deterministic "
                          "backward)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="record the DRAM bytes per launch of an ncu --csv capture (metrics "
+                         "dram__bytes_read.sum, dram__bytes_write.sum) taken on --workload "
+                         "into profiles/dram_traffic.json, then exit")
+    ap.add_argument("--record-command", default="",
+                    help="the ncu command line the capture came from (stored beside it)")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic, args.workload, args.record_command)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

@@ -18,8 +18,14 @@
 //   - Calls that can overlap on the GPU (different streams, or different host
 //     threads without ordering) race on the array and give wrong gradients.
 //     Order them on one stream, or synchronise between them.
-//   - The array exists on every device where this library's entry point has
-//     been called, from that first call until the process exits.
+//   - The array occupies device memory on every device where this library's
+//     module is loaded, until the process exits.  With lazy module loading
+//     (the CUDA default) that happens at the first call into the library on
+//     a device; with CUDA_MODULE_LOADING=EAGER the array is reserved when the
+//     context is created, whether or not attn_bwd_noalloc is ever called.
+//   - The cached address (below) belongs to the device's current context.
+//     cudaDeviceReset destroys that context: do not use this library across
+//     a cudaDeviceReset (the error word of attn_api.cu is cached the same way).
 //   - In host code the array's name is only a host-side stand-in, never a
 //     device address.  The first call on each device (with that device current)
 //     looks the real address up once with cudaGetSymbolAddress and caches it;

@@ -239,8 +239,12 @@ int attn_bwd_deterministic(const void* q, const void* k, const void* v, const vo
  *     reads before reading it.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it: make it before any stream capture.
- *   - The array occupies device memory from the first call on a device until
- *     the process exits.
+ *   - The array occupies device memory until the process exits: from the
+ *     first call into this library on a device under lazy module loading (the
+ *     CUDA default), or from context creation on every device when
+ *     CUDA_MODULE_LOADING=EAGER, even if attn_bwd_noalloc is never called.
+ *   - The library caches per-device addresses (this array, its error word):
+ *     do not use it across cudaDeviceReset.
  */
 int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, int B, int Hq, int Hkv, int N, int D, int causal,

@@ -130,9 +130,11 @@ def test_noalloc_backward_rejects_problems_beyond_its_fixed_scratch():
     lib = binding.load()
     limit = lib.attn_bwd_noalloc_scratch_limit()
     assert limit == 32 << 20
-    # B=1, H=16, N=8192, D=128 needs 16*8192*130*4 bytes > 32 MiB
-    st = lib.attn_bwd_noalloc(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 16, 16, 8192, 128, 0,
-                              0.08, None, 0x6000, 0x7000, 0x8000, 0x9000)
+    # B=1, H=16, N=8192, D=128 needs 16*8192*130*4 bytes > 32 MiB.  Null
+    # pointers: the size check comes first; were it ever moved after the
+    # pointer checks, the call would return INVALID_ARG, never launch.
+    st = lib.attn_bwd_noalloc(None, None, None, None, None, 1, 16, 16, 8192, 128, 0,
+                              0.08, None, None, None, None, None)
     assert st == binding.ATTN_ERR_SCRATCH_LIMIT
     assert "scratch" in binding.status_text(st)
 
