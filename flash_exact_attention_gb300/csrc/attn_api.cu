@@ -186,6 +186,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
     const long long tiles = (long long)((N + 127) / 128) * B * Hq;
     const int sms = device_sm_count(dev);
     p.kvsplit = ((long long)p.num_qblocks * B * Hq < sms) && (causal != 0 || tiles <= sms);
+    p.ctas = sms;
   }
   p.num_kv_tiles = (N + 127) / 128;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -242,6 +243,7 @@ int fwd_varlen_entry(const void* q, const void* k, const void* v, void* o, float
   p.steps = 0;
   p.cu_seqlens = cu_seqlens;
   p.total = total;
+  p.ctas = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool c = causal != 0;
   // (the packed maps only copy 16-bit elements: the same for bf16 and fp16)
@@ -290,6 +292,7 @@ int stj_entry(const void* q, const void* k, const void* v, void* o, float* pole,
   p.steps = steps;
   p.cu_seqlens = nullptr;
   p.total = 0;
+  p.ctas = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = (D == 64) ? launch_stj_d64(tq, tk, tv, p, causal != 0, order, s)
                             : launch_stj_d128(tq, tk, tv, p, causal != 0, order, s);

@@ -2,10 +2,13 @@
 //
 // Work partition ("From-scratch CUDA attention kernel reaches 94.4% of
 // FlashAttention-4 on NVIDIA B200", section "How the kernel partitions its
-// work"): Q, K, V and O are cut into 128-row tiles; each CTA owns one
-// (batch, query head) and TWO consecutive 128-row Q tiles, loads them once,
-// and streams the K/V tiles of its key/value head through a shared-memory
-// ring.  For each K/V tile: S = Q K^T (tensor cores, fp32 in TMEM), an online
+// work"): Q, K, V and O are cut into 128-row tiles; a work unit is one
+// (batch, query head) and TWO consecutive 128-row Q tiles, loaded once, whose
+// K/V tiles stream through a shared-memory ring.  One CTA per unit, except
+// in the split-key mode with more units than SMs (PERSIST): there at most one
+// CTA per SM walks its share of the units (see unit_index), so barriers and
+// TMEM are set up once per CTA and the next unit's Q and K/V loads overlap the
+// current unit's last steps and epilogue.  For each K/V tile: S = Q K^T (tensor cores, fp32 in TMEM), an online
 // softmax update (running row max m and running row sum l, FlashStieltjes
 // page, "The challenge"), P (bf16, written back over S in TMEM), and
 // O += P V (tensor cores, fp32 in TMEM).  At the end O / l is written as bf16
@@ -59,8 +62,9 @@ struct FwdCfg {
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  // barriers: q_full, full[kStages], empty[kStages], s_full[2], p_full[2], o_final
-  static constexpr int kNumBars = 1 + 2 * kStages + 5;
+  // barriers: q_full, full[kStages], empty[kStages], s_full[2], p_full[2], o_final,
+  // q_empty, o_free[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 8;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + misc + alignment slack
   static constexpr int kThreads = 384;
   // Register split (per thread): 8 softmax warps, 4 other warps.
@@ -70,68 +74,128 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
 };
 
+// Position in the K/V ring: stage and the parity of its current use,
+// advanced one entry at a time (no division by the stage count).
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;
+  template <int ST>
+  __device__ __forceinline__ void advance() {
+    if (++s == ST) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// One work unit: query tiles t0 (slot 0) and t1 (slot 1) of one (batch, query
+// head); n0 / n1 key tiles for the two slots (KVSPLIT: t0 == t1, slot 0 takes
+// key tiles [0, h0), slot 1 [h0, h0 + n1)).
+struct FwdUnit {
+  int bh, b, h, bh_kv;
+  int seq0, N;  // first token and length of the unit's sequence
+  int t0, t1, h0, n0, n1, nkv;
+  bool has_t1;
+};
+
 // VARLEN: a batch of sequences of different lengths packed token-major,
 // q/o [total, Hq, D], k/v [total, Hkv, D], lse [Hq, total]; sequence b is
 // rows cu_seqlens[b] .. cu_seqlens[b+1]-1.  The grid is that of a batch of
-// max_seqlen-long sequences (p.N = max_seqlen); CTAs past their sequence's
-// end leave at once.  The TMA maps address a head's rows with a stride of
-// H*D elements (box 64 x 1 head x 128 tokens), which lands in shared memory
-// exactly as a dense tile; key rows past the sequence are masked like a
-// ragged tail and query rows past it are not written.
+// max_seqlen-long sequences (p.N = max_seqlen), one unit per CTA; CTAs past
+// their sequence's end leave at once.  The TMA maps address a head's rows
+// with a stride of H*D elements (box 64 x 1 head x 128 tokens), which lands in
+// shared memory exactly as a dense tile; key rows past the sequence are masked
+// like a ragged tail and query rows past it are not written.
 //
-// KVSPLIT: one 128-row query tile per CTA, its key range cut in two halves
+// KVSPLIT: one 128-row query tile per unit, its key range cut in two halves
 // that the two tile slots (TMEM S/O pairs, softmax warpgroups) process side
 // by side -- slot 0 key tiles [0, n/2), slot 1 [n/2, n) -- and merged at the
-// end from each slot's (max, sum, O).  For grids of less than one wave:
-// every step keeps both slots busy and the longest CTA runs about n/2 steps,
-// where pairing query tiles t and T-1-t (so that every CTA runs T+1 steps)
-// leaves one slot idle in most steps.
-template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool KVSPLIT = false>
+// end from each slot's (max, sum, O).  For grids of less than one wave of
+// tile pairs: every step keeps both slots busy and the longest unit runs
+// about n/2 steps, where pairing query tiles t and T-1-t (so that every unit
+// runs T+1 steps) leaves one slot idle in most steps.
+//
+// PERSIST (split-key mode only): at most one CTA per SM, each walking its
+// units (see unit_index); the host uses it when there are more units than
+// SMs, so that a CTA's second unit's set-up and first loads hide under its
+// first unit's last steps.  Otherwise every CTA runs one unit.
+template <int D, bool CAUSAL, bool F16, bool VARLEN = false, bool KVSPLIT = false,
+          bool PERSIST = false>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D>;
   static_assert(!KVSPLIT || !VARLEN, "KVSPLIT is a mode of the dense kernel");
+  static_assert(!PERSIST || KVSPLIT, "persistent CTAs are used in the split-key mode");
   constexpr int ST = Cfg::kStages;
 
-  // ---- work unit: two 128-row query tiles t0 < t1 of one (batch, head).
-  //  * Non-causal: adjacent tiles (2qb, 2qb+1); the CTAs of one head are
-  //    consecutive so that those resident at one time share its K/V in L2.
+  // ---- work units, in the order of their index u:
+  //  * Non-causal: adjacent tiles (2qb, 2qb+1); the units of one head are
+  //    consecutive so that those in flight at one time share its K/V in L2.
   //  * Causal: adjacent tiles, longest blocks of all heads first (both tiles
   //    are active in almost every step, so the MMAs of one overlap the
   //    softmax of the other).
-  //  * KVSPLIT: qb is the CTA's one query tile, longest first when causal.
+  //  * KVSPLIT: qb is the unit's one query tile, longest first when causal.
   const int BH = p.B * p.Hq;
   const int nqb = KVSPLIT ? p.num_kv_tiles : p.num_qblocks;
-  const int qb = CAUSAL ? nqb - 1 - (int)blockIdx.x / BH : (int)blockIdx.x % nqb;
-  const int bh = CAUSAL ? (int)blockIdx.x % BH : (int)blockIdx.x / nqb;
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int bh_kv = b * p.Hkv + h / p.G;
-  int seq0 = 0, N = p.N;  // first token and length of this CTA's sequence
+  const int units = nqb * BH;
+  const int G = (int)gridDim.x;
+  // Units per CTA: several only with PERSIST, in the split-key mode (grids
+  // of tile pairs under one wave), where each CTA has one or two units.
+  // Grids of tile pairs keep one unit per CTA: with several units per CTA
+  // the static assignment measured 2-4 % slower than the hardware's dispatch
+  // of whole CTAs to the SMs that free up first.
+  constexpr bool kPersist = PERSIST;
+  constexpr int kMaxUnits = kPersist ? 0x7FFFFFFF : 1;
+  // The k-th unit of this CTA: rounds of G consecutive units, walked forwards
+  // in even rounds and backwards in odd ones, so that (longest first) the
+  // CTA that took a round's longest unit takes the next round's shortest.
+  // A packed batch (VARLEN) keeps one unit per CTA: its lengths are known on
+  // the device only.
+  auto unit_index = [&](int k) -> int {
+    if (!kPersist) return k == 0 ? (int)blockIdx.x : -1;
+    const int r = k * G + ((k & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    return r < units ? r : -1;
+  };
+  auto decode = [&](int u) {
+    FwdUnit U;
+    const int qb = CAUSAL ? nqb - 1 - u / BH : u % nqb;
+    U.bh = CAUSAL ? u % BH : u / nqb;
+    U.b = U.bh / p.Hq;
+    U.h = U.bh % p.Hq;
+    U.bh_kv = U.b * p.Hkv + U.h / p.G;
+    U.seq0 = 0;
+    U.N = p.N;
+    if constexpr (VARLEN) {
+      U.seq0 = p.cu_seqlens[U.b];
+      U.N = p.cu_seqlens[U.b + 1] - U.seq0;
+    }
+    const int T = VARLEN ? (U.N + 127) / 128 : p.num_kv_tiles;
+    U.t0 = KVSPLIT ? qb : 2 * qb;
+    U.t1 = KVSPLIT ? qb : 2 * qb + 1;
+    U.has_t1 = KVSPLIT || U.t1 * 128 < U.N;
+    const int n_all = CAUSAL ? qb + 1 : T;  // KVSPLIT: the query tile's key tiles
+    U.h0 = KVSPLIT ? n_all / 2 : 0;
+    U.n0 = KVSPLIT ? U.h0 : (CAUSAL ? U.t0 + 1 : T);
+    U.n1 = KVSPLIT ? n_all - U.h0 : (U.has_t1 ? (CAUSAL ? U.t1 + 1 : T) : 0);
+    U.nkv = max(U.n0, U.n1);
+    return U;
+  };
+  // The CTA's first unit, decoded by every thread before the set-up (the
+  // integer divisions overlap it); later units are decoded by each role.
+  const FwdUnit U0 = decode((int)blockIdx.x);
   if constexpr (VARLEN) {
-    seq0 = p.cu_seqlens[b];
-    N = p.cu_seqlens[b + 1] - seq0;
     // lengths must lie in [0, max_seqlen] and sequences inside [0, total)
-    if (seq0 < 0 || N < 0 || N > p.N || seq0 > p.total - N) {
+    if (U0.seq0 < 0 || U0.N < 0 || U0.N > p.N || U0.seq0 > p.total - U0.N) {
       if (threadIdx.x == 0) atomicOr(p.err, kErrSeqlen);
       return;
     }
-    if (2 * qb * 128 >= N) return;  // past this sequence's end
+    if (U0.t0 * 128 >= U0.N) return;  // past this sequence's end
   }
-  const int T = VARLEN ? (N + 127) / 128 : p.num_kv_tiles;
-  const int t0 = KVSPLIT ? qb : 2 * qb;
-  const int t1 = KVSPLIT ? qb : 2 * qb + 1;
-  const bool has_t1 = KVSPLIT || t1 * 128 < N;
-  // KVSPLIT: the query tile's n_all key tiles, slot 1 starting at tile h0
-  const int n_all = CAUSAL ? qb + 1 : T;
-  const int h0 = KVSPLIT ? n_all / 2 : 0;
-  const int n0 = KVSPLIT ? h0 : (CAUSAL ? t0 + 1 : T);
-  const int n1 = KVSPLIT ? n_all - h0 : (has_t1 ? (CAUSAL ? t1 + 1 : T) : 0);
-  const int nkv = max(n0, n1);
   // TMA coordinates of a 128-row tile: (column, row, plane) of the dense
   // (D, N, B*H) map, or (column, head, token) of the packed (D, H, total) map
   auto load_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c, int tile,
-                       int plane, int head) {
+                       int plane, int head, int seq0) {
     if constexpr (VARLEN)
       tma_load_3d(dst, tm, bar, c * 64, head, seq0 + tile * 128);
     else
@@ -152,7 +216,9 @@ __global__ void __launch_bounds__(384, 1)
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + ST + s); };
   auto bar_s = [&](int t) { return bar0 + 8u * (1 + 2 * ST + t); };
   auto bar_p = [&](int t) { return bar0 + 8u * (3 + 2 * ST + t); };
-  auto bar_o = [&]() { return bar0 + 8u * (5 + 2 * ST); };
+  auto bar_o = [&]() { return bar0 + 8u * (5 + 2 * ST); };       // a unit's MMAs all done
+  auto bar_qe = [&]() { return bar0 + 8u * (6 + 2 * ST); };      // a unit's S MMAs all done
+  auto bar_of = [&](int t) { return bar0 + 8u * (7 + 2 * ST + t); };  // O_t read out
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kBarOff + Cfg::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -165,8 +231,11 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
       mbar_init(bar_p(t), 4);
+      // KVSPLIT: both warpgroups read both O accumulators in the merge
+      mbar_init(bar_of(t), KVSPLIT ? 8 : 4);
     }
     mbar_init(bar_o(), 1);
+    mbar_init(bar_qe(), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -186,39 +255,49 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ TMA producer
     regs_decrease<Cfg::kRegOther>();
     if (lane == 0) {
-      const int nq = (has_t1 && !KVSPLIT) ? 2 : 1;
-      mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
-      for (int t = 0; t < nq; ++t)
-        for (int c = 0; c < Cfg::kBoxes; ++c)
-          load_tile(sbase + Cfg::kQOff + t * Cfg::kTileBytes + c * Cfg::kBoxBytes, &tm_q, bar_q(),
-                    c, t ? t1 : t0, bh, h);
-      uint32_t it = 0;
+      uint32_t it = 0;  // ring entries issued (over all units)
+      RingPos rp;       // ring position of entry `it`
+      int nql = 0;      // Q loads issued
       bool ok = true;
-      for (int j = 0; j < nkv && ok; ++j) {
-        // Ring entries of step j: K_j, V_j; with KVSPLIT K of slot 0 (while it
-        // is active) and of slot 1, then V of slot 0 and of slot 1.
-        for (int e = 0; e < (KVSPLIT ? 4 : 2) && ok; ++e) {
-          const int kv = KVSPLIT ? (e >> 1) : e;
-          const int slot = e & 1;
-          if (KVSPLIT && slot == 0 && j >= n0) continue;
-          const int tile = (KVSPLIT && slot) ? h0 + j : j;
-          const int s = (int)(it % ST);
-          const uint32_t ph = (it / ST) & 1u;
-          ok = mbar_wait_inl(bar_empty(s), ph ^ 1u, wc);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bar_full(s), Cfg::kTileBytes);
-          const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+      for (int k = 0; k < kMaxUnits && ok; ++k) {
+        const int u = unit_index(k);
+        if (u < 0) break;
+        const FwdUnit U = k == 0 ? U0 : decode(u);
+        // The unit's Q tiles replace the previous unit's once its S MMAs are done.
+        if (k > 0 && !(ok = mbar_wait_tested_inl(bar_qe(), (uint32_t)(k - 1) & 1u, wc))) break;
+        const int nq = (U.has_t1 && !KVSPLIT) ? 2 : 1;
+        mbar_arrive_expect_tx(bar_q(), nq * Cfg::kTileBytes);
+        for (int t = 0; t < nq; ++t)
           for (int c = 0; c < Cfg::kBoxes; ++c)
-            load_tile(sbase + Cfg::kRingOff + s * Cfg::kTileBytes + c * Cfg::kBoxBytes, tm,
-                      bar_full(s), c, tile, bh_kv, h / p.G);
-          ++it;
+            load_tile(sbase + Cfg::kQOff + t * Cfg::kTileBytes + c * Cfg::kBoxBytes, &tm_q,
+                      bar_q(), c, t ? U.t1 : U.t0, U.bh, U.h, U.seq0);
+        ++nql;
+        for (int j = 0; j < U.nkv && ok; ++j) {
+          // Ring entries of step j: K_j, V_j; with KVSPLIT K of slot 0 (while it
+          // is active) and of slot 1, then V of slot 0 and of slot 1.
+          for (int e = 0; e < (KVSPLIT ? 4 : 2) && ok; ++e) {
+            const int kv = KVSPLIT ? (e >> 1) : e;
+            const int slot = e & 1;
+            if (KVSPLIT && slot == 0 && j >= U.n0) continue;
+            const int tile = (KVSPLIT && slot) ? U.h0 + j : j;
+            const int s = rp.s;
+            ok = mbar_wait_inl(bar_empty(s), rp.ph ^ 1u, wc);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar_full(s), Cfg::kTileBytes);
+            const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+            for (int c = 0; c < Cfg::kBoxes; ++c)
+              load_tile(sbase + Cfg::kRingOff + s * Cfg::kTileBytes + c * Cfg::kBoxBytes, tm,
+                        bar_full(s), c, tile, U.bh_kv, U.h / p.G, U.seq0);
+            ++it;
+            rp.advance<ST>();
+          }
         }
       }
       if (!ok) {
         // Let every copy already issued land before the CTA can exit.
         for (uint32_t f = (it > (uint32_t)ST ? it - ST : 0); f < it; ++f)
           mbar_wait_drain_inl(bar_full((int)(f % ST)), (f / ST) & 1u, wc);
-        mbar_wait_drain_inl(bar_q(), 0, wc);
+        if (nql > 0) mbar_wait_drain_inl(bar_q(), (uint32_t)(nql - 1) & 1u, wc);
       }
     }
   } else if (warp == 9) {
@@ -254,117 +333,149 @@ __global__ void __launch_bounds__(384, 1)
                    (acc || kk > 0) ? 1u : 0u);
       };
 
-      bool ok = mbar_wait_inl(bar_q(), 0, wc);
-      uint32_t it = 0, np0 = 0, np1 = 0;
-      int sv_prev = 0;
-      bool a1_prev = false;
-      if constexpr (KVSPLIT) {
-        // Order per step j, consuming the ring entries in the producer's order
-        // K_0(j), K_1(j), V_0(j), V_1(j): S_0(j); O_1 += P_1(j-1) V_1(j-1);
-        // S_1(j); O_0 += P_0(j) V_0(j) -- each softmax gets the duration of
-        // the other slot's two MMAs, as with two query tiles.
-        auto next = [&](int& s, uint32_t& ph) {
-          s = (int)(it % ST);
-          ph = (it / ST) & 1u;
-          ++it;
-        };
-        int svb = 0;
-        uint32_t phvb = 0;
-        for (int j = 0; j < nkv && ok; ++j) {
-          const bool a0 = j < n0;
-          int s;
-          uint32_t ph;
-          if (a0) {
+      bool ok = true;
+      uint32_t np0 = 0, np1 = 0;
+      RingPos rp;  // next ring entry to consume
+      int k = 0;
+      for (; k < kMaxUnits && ok; ++k) {
+        const int u = unit_index(k);
+        if (u < 0) break;
+        const FwdUnit U = k == 0 ? U0 : decode(u);
+        const int n0 = U.n0, n1 = U.n1, nkv = U.nkv;
+        if (!(ok = mbar_wait_inl(bar_q(), (uint32_t)k & 1u, wc))) break;
+        // A unit's first P.V MMA of slot t overwrites O_t: the softmax warps must
+        // have read the previous unit's O_t out of TMEM (phase k-1 of bar_of(t)).
+        const uint32_t of_ph = (uint32_t)(k - 1) & 1u;
+        bool of0 = k == 0, of1 = k == 0;
+        int sv_prev = 0;
+        bool a1_prev = false;
+        if constexpr (KVSPLIT) {
+          // Order per step j, consuming the ring entries in the producer's order
+          // K_0(j), K_1(j), V_0(j), V_1(j): S_0(j); O_1 += P_1(j-1) V_1(j-1);
+          // S_1(j); O_0 += P_0(j) V_0(j) -- each softmax gets the duration of
+          // the other slot's two MMAs, as with two query tiles.
+          auto next = [&](int& s, uint32_t& ph) {
+            s = rp.s;
+            ph = rp.ph;
+            rp.advance<ST>();
+          };
+          int svb = 0;
+          uint32_t phvb = 0;
+          for (int j = 0; j < nkv && ok; ++j) {
+            const bool a0 = j < n0;
+            int s;
+            uint32_t ph;
+            if (a0) {
+              next(s, ph);
+              if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
+              tc_fence_after();
+              issue_qk(0, ring(s));
+              mma_commit(bar_s(0));
+              mma_commit(bar_empty(s));
+            }
+            if (j > 0) {
+              if (!(ok = mbar_wait_inl(bar_full(svb), phvb, wc))) break;
+              if (!(ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) break;
+              if (!of1 && !(ok = mbar_wait_inl(bar_of(1), of_ph, wc))) break;
+              of1 = true;
+              ++np1;
+              tc_fence_after();
+              issue_pv(1, ring(svb), j - 1 > 0);
+              mma_commit(bar_empty(svb));
+            }
             next(s, ph);
             if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
             tc_fence_after();
-            issue_qk(0, ring(s));
-            mma_commit(bar_s(0));
+            issue_qk(1, ring(s));
+            mma_commit(bar_s(1));
             mma_commit(bar_empty(s));
+            if (a0) {
+              next(s, ph);
+              if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
+              if (!(ok = mbar_wait_inl(bar_p(0), np0 & 1u, wc))) break;
+              if (!of0 && !(ok = mbar_wait_inl(bar_of(0), of_ph, wc))) break;
+              of0 = true;
+              ++np0;
+              tc_fence_after();
+              issue_pv(0, ring(s), j > 0);
+              mma_commit(bar_empty(s));
+            }
+            next(svb, phvb);  // V_1(j): waited for where it is used
           }
-          if (j > 0) {
-            if (!(ok = mbar_wait_inl(bar_full(svb), phvb, wc))) break;
+          if (ok) mma_commit(bar_qe());  // every S MMA of the unit is issued
+          if (ok && nkv > 0) {
+            ok = mbar_wait_inl(bar_full(svb), phvb, wc) && mbar_wait_inl(bar_p(1), np1 & 1u, wc) &&
+                 (of1 || mbar_wait_inl(bar_of(1), of_ph, wc));
+            if (ok) {
+              ++np1;
+              tc_fence_after();
+              issue_pv(1, ring(svb), nkv - 1 > 0);
+              mma_commit(bar_empty(svb));
+            }
+          }
+        }
+        for (int j = 0; j < (KVSPLIT ? 0 : nkv) && ok; ++j) {
+          const bool a0 = j < n0, a1 = j < n1;
+          const int sk = rp.s;
+          const uint32_t phk = rp.ph;
+          rp.advance<ST>();
+          const int sv = rp.s;
+          const uint32_t phv = rp.ph;
+          rp.advance<ST>();
+          if (!(ok = mbar_wait_inl(bar_full(sk), phk, wc))) break;
+          tc_fence_after();
+          if (a0) {
+            issue_qk(0, ring(sk));
+            mma_commit(bar_s(0));
+          }
+          if (j > 0 && a1_prev) {
             if (!(ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) break;
+            if (!of1 && !(ok = mbar_wait_inl(bar_of(1), of_ph, wc))) break;
+            of1 = true;
             ++np1;
             tc_fence_after();
-            issue_pv(1, ring(svb), j - 1 > 0);
-            mma_commit(bar_empty(svb));
+            issue_pv(1, ring(sv_prev), j - 1 > 0);
           }
-          next(s, ph);
-          if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
+          if (j > 0) mma_commit(bar_empty(sv_prev));
+          if (a1) {
+            issue_qk(1, ring(sk));
+            mma_commit(bar_s(1));
+          }
+          mma_commit(bar_empty(sk));
+          if (!(ok = mbar_wait_inl(bar_full(sv), phv, wc))) break;
           tc_fence_after();
-          issue_qk(1, ring(s));
-          mma_commit(bar_s(1));
-          mma_commit(bar_empty(s));
           if (a0) {
-            next(s, ph);
-            if (!(ok = mbar_wait_inl(bar_full(s), ph, wc))) break;
             if (!(ok = mbar_wait_inl(bar_p(0), np0 & 1u, wc))) break;
+            if (!of0 && !(ok = mbar_wait_inl(bar_of(0), of_ph, wc))) break;
+            of0 = true;
             ++np0;
             tc_fence_after();
-            issue_pv(0, ring(s), j > 0);
-            mma_commit(bar_empty(s));
+            issue_pv(0, ring(sv), j > 0);
           }
-          next(svb, phvb);  // V_1(j): waited for where it is used
+          sv_prev = sv;
+          a1_prev = a1;
         }
-        if (ok && nkv > 0) {
-          ok = mbar_wait_inl(bar_full(svb), phvb, wc) && mbar_wait_inl(bar_p(1), np1 & 1u, wc);
-          if (ok) {
-            ++np1;
-            tc_fence_after();
-            issue_pv(1, ring(svb), nkv - 1 > 0);
-            mma_commit(bar_empty(svb));
+        if (!KVSPLIT && ok) {
+          mma_commit(bar_qe());  // every S MMA of the unit is issued
+          if (a1_prev) {
+            if ((ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc) &&
+                      (of1 || mbar_wait_inl(bar_of(1), of_ph, wc)))) {
+              ++np1;
+              tc_fence_after();
+              issue_pv(1, ring(sv_prev), nkv - 1 > 0);
+            }
           }
+          // the last V tile: no S MMA of this unit reads the ring after it
+          if (ok && nkv > 0) mma_commit(bar_empty(sv_prev));
         }
+        if (ok) mma_commit(bar_o());
       }
-      for (int j = 0; j < (KVSPLIT ? 0 : nkv) && ok; ++j) {
-        const bool a0 = j < n0, a1 = j < n1;
-        const int sk = (int)(it % ST);
-        const uint32_t phk = (it / ST) & 1u;
-        ++it;
-        const int sv = (int)(it % ST);
-        const uint32_t phv = (it / ST) & 1u;
-        ++it;
-        if (!(ok = mbar_wait_inl(bar_full(sk), phk, wc))) break;
-        tc_fence_after();
-        if (a0) {
-          issue_qk(0, ring(sk));
-          mma_commit(bar_s(0));
-        }
-        if (j > 0 && a1_prev) {
-          if (!(ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) break;
-          ++np1;
-          tc_fence_after();
-          issue_pv(1, ring(sv_prev), j - 1 > 0);
-        }
-        if (j > 0) mma_commit(bar_empty(sv_prev));
-        if (a1) {
-          issue_qk(1, ring(sk));
-          mma_commit(bar_s(1));
-        }
-        mma_commit(bar_empty(sk));
-        if (!(ok = mbar_wait_inl(bar_full(sv), phv, wc))) break;
-        tc_fence_after();
-        if (a0) {
-          if (!(ok = mbar_wait_inl(bar_p(0), np0 & 1u, wc))) break;
-          ++np0;
-          tc_fence_after();
-          issue_pv(0, ring(sv), j > 0);
-        }
-        sv_prev = sv;
-        a1_prev = a1;
-      }
-      if (ok && a1_prev) {
-        if ((ok = mbar_wait_inl(bar_p(1), np1 & 1u, wc))) {
-          ++np1;
-          tc_fence_after();
-          issue_pv(1, ring(sv_prev), nkv - 1 > 0);
-        }
-      }
-      mma_commit(bar_o());
       // On an aborted run nobody else may wait for the final commit: wait here
       // so that no MMA is in flight when TMEM is released.
-      if (!ok) mbar_wait_drain_inl(bar_o(), 0, wc);
+      if (!ok) {
+        mma_commit(bar_o());
+        mbar_wait_drain_inl(bar_o(), (uint32_t)k & 1u, wc);
+      }
     }
   } else if (warp >= 10) {
     regs_decrease<Cfg::kRegOther>();
@@ -374,165 +485,191 @@ __global__ void __launch_bounds__(384, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const int n_t = t ? n1 : n0;
-    const int qtile = t ? t1 : t0;
-    const int grow = qtile * 128 + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem_base + lane_off + 256u + (uint32_t)(t * 128);
     const float C = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
+    uint32_t ns = 0;  // S tiles of this slot waited for (over all units)
     bool ok = true;
-    for (int j = 0; j < n_t; ++j) {
-      // tcgen05.ld/st are warp-collective: keep the decision warp-uniform.
-      ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_s(t), (uint32_t)j & 1u, wc));
-      if (!ok) break;
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t r[4][32];
+    for (int k = 0; k < kMaxUnits && ok; ++k) {
+      const int u = unit_index(k);
+      if (u < 0) break;
+      const FwdUnit U = k == 0 ? U0 : decode(u);
+      const int n_t = t ? U.n1 : U.n0;
+      const int qtile = t ? U.t1 : U.t0;
+      const int grow = qtile * 128 + row;
+      const int N = U.N;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_t; ++j) {
+        // tcgen05.ld/st are warp-collective: keep the decision warp-uniform.
+        ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_s(t), ns & 1u, wc));
+        ++ns;
+        if (!ok) break;
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t r[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
-        tmem_ld_wait();
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, r[c]);
+          tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[c][i]);
+        }
+        const int kvt = (KVSPLIT && t) ? U.h0 + j : j;  // key tile of this step
+        const int kv0 = kvt * 128;
+        if ((CAUSAL && kvt == qtile) || kv0 + 128 > N) {
+          int lim = N - kv0;  // columns >= lim are past the sequence end
+          if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // causal: key <= query
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        float mp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mp[q] = fmaxf(s[q], s[q + 8]);
+#pragma unroll
+        for (int c = 16; c < 128; c += 16)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mp[q] = fmax3(mp[q], s[c + q], s[c + 8 + q]);
+        const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]),
+                               fmaxf(mp[6], mp[7]));
+        const float m_new = fmaxf(m_used, mx * C);
+        const bool need = (m_new - m_used) > kRescaleThreshold;
+        const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
+        if (need) m_used = m_new;
+        l *= corr;
+        const float2 c2 = make_float2(C, C);
+        const float2 nm2 = make_float2(-m_used, -m_used);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, nm2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pp);
+          pk[c / 2] = pack2<F16>(pp.x, pp.y);
+          if (c == 62) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        }
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l += a.x + a.y;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O_t is stable here: its last update was committed before S_t(j).
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tO + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+            tmem_st32(tO + c, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p(t));
       }
-      const int kvt = (KVSPLIT && t) ? h0 + j : j;  // key tile of this step
-      const int kv0 = kvt * 128;
-      if ((CAUSAL && kvt == qtile) || kv0 + 128 > N) {
-        int lim = N - kv0;  // columns >= lim are past the sequence end
-        if (CAUSAL) lim = min(lim, grow - kv0 + 1);  // causal: key <= query
+      // Every warp waits for the unit's MMAs, with or without steps of its own,
+      // so that all roles move from unit to unit together.
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), (uint32_t)k & 1u, wc));
+      if constexpr (KVSPLIT) {
+        // Merge the two slots' partial results of the same rows: each thread
+        // publishes its (m, l) through the unused second Q buffer; then
+        // warpgroup t writes output columns [t D/2, (t+1) D/2) and warpgroup 0
+        // the LSE.  Both warpgroups pass this named barrier once per unit, the
+        // shared decision included, so they leave the unit loop together.
+        float* xm = reinterpret_cast<float*>(smem + Cfg::kQOff + Cfg::kTileBytes);
+        xm[(2 * t) * 128 + row] = m_used;
+        xm[(2 * t + 1) * 128 + row] = l;
+        ok = named_bar_and(1, 256, ok);
+        if (ok) {
+          tc_fence_after();
+          const int n0 = U.n0;
+          const float m0 = xm[row], l0 = xm[128 + row], m1 = xm[256 + row], l1 = xm[384 + row];
+          const float m = n0 > 0 ? fmaxf(m0, m1) : m1;
+          const float a0 = n0 > 0 ? ex2_approx(m0 - m) : 0.f;
+          const float a1 = ex2_approx(m1 - m);
+          const float L = a0 * l0 + a1 * l1;
+          const float s0 = a0 / L, s1 = a1 / L;
+          const bool live = grow < N;
+          uint4* orow = reinterpret_cast<uint4*>(
+              static_cast<uint16_t*>(p.o) + ((size_t)U.bh * p.N + (size_t)(live ? grow : 0)) * D);
+          const uint32_t tO0 = tmem_base + lane_off + 256u, tO1 = tmem_base + lane_off + 384u;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) s[c] = -INFINITY;
+          for (int c = t * (D / 2); c < (t + 1) * (D / 2); c += 32) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tO1 + c, r1);
+            if (n0 > 0) tmem_ld32(tO0 + c, r0);
+            tmem_ld_wait();
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              o[i] = __uint_as_float(r1[i]) * s1 + (n0 > 0 ? __uint_as_float(r0[i]) * s0 : 0.f);
+            if (live) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = pack2<F16>(o[8 * v + 0], o[8 * v + 1]);
+                w.y = pack2<F16>(o[8 * v + 2], o[8 * v + 3]);
+                w.z = pack2<F16>(o[8 * v + 4], o[8 * v + 5]);
+                w.w = pack2<F16>(o[8 * v + 6], o[8 * v + 7]);
+                orow[c / 8 + v] = w;
+              }
+            }
+          }
+          if (t == 0 && live)
+            p.lse[(size_t)U.bh * p.N + grow] = (m + log2f(L)) * 0.69314718055994530942f;
+        }
       }
-      float mp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = fmaxf(s[k], s[k + 8]);
-#pragma unroll
-      for (int c = 16; c < 128; c += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mp[k] = fmax3(mp[k], s[c + k], s[c + 8 + k]);
-      const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]),
-                             fmaxf(mp[6], mp[7]));
-      const float m_new = fmaxf(m_used, mx * C);
-      const bool need = (m_new - m_used) > kRescaleThreshold;
-      const float corr = need ? ex2_approx(m_used - m_new) : 1.f;
-      if (need) m_used = m_new;
-      l *= corr;
-      const float2 c2 = make_float2(C, C);
-      const float2 nm2 = make_float2(-m_used, -m_used);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, nm2);
-        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], pp);
-        pk[c / 2] = pack2<F16>(pp.x, pp.y);
-        if (c == 62) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      }
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a = __fadd2_rn(a01, a23);
-      l += a.x + a.y;
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O_t is stable here: its last update was committed before S_t(j).
+      if (!KVSPLIT && ok && n_t > 0) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const bool live = grow < N;
+        // row grow of the output: dense [B*Hq, N, D], or packed [total, Hq, D]
+        const size_t orow_idx = VARLEN ? ((size_t)(U.seq0 + (live ? grow : 0)) * p.Hq + U.h)
+                                       : ((size_t)U.bh * p.N + (size_t)(live ? grow : 0));
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * D);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t r[32];
           tmem_ld32(tO + c, r);
           tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-          tmem_st32(tO + c, r);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p(t));
-    }
-    if constexpr (KVSPLIT) {
-      // Merge the two slots' partial results of the same rows: each thread
-      // publishes its (m, l) through the unused second Q buffer; then
-      // warpgroup t writes output columns [t D/2, (t+1) D/2) and warpgroup 0
-      // the LSE.
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), 0, wc));
-      float* xm = reinterpret_cast<float*>(smem + Cfg::kQOff + Cfg::kTileBytes);
-      xm[(2 * t) * 128 + row] = m_used;
-      xm[(2 * t + 1) * 128 + row] = l;
-      ok = named_bar_and(1, 256, ok);
-      if (ok) {
-        tc_fence_after();
-        const float m0 = xm[row], l0 = xm[128 + row], m1 = xm[256 + row], l1 = xm[384 + row];
-        const float m = n0 > 0 ? fmaxf(m0, m1) : m1;
-        const float a0 = n0 > 0 ? ex2_approx(m0 - m) : 0.f;
-        const float a1 = ex2_approx(m1 - m);
-        const float L = a0 * l0 + a1 * l1;
-        const float s0 = a0 / L, s1 = a1 / L;
-        const bool live = grow < N;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                               ((size_t)bh * p.N + (size_t)(live ? grow : 0)) * D);
-        const uint32_t tO0 = tmem_base + lane_off + 256u, tO1 = tmem_base + lane_off + 384u;
-#pragma unroll
-        for (int c = t * (D / 2); c < (t + 1) * (D / 2); c += 32) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tO1 + c, r1);
-          if (n0 > 0) tmem_ld32(tO0 + c, r0);
-          tmem_ld_wait();
-          float o[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            o[i] = __uint_as_float(r1[i]) * s1 + (n0 > 0 ? __uint_as_float(r0[i]) * s0 : 0.f);
           if (live) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 w;
-              w.x = pack2<F16>(o[8 * v + 0], o[8 * v + 1]);
-              w.y = pack2<F16>(o[8 * v + 2], o[8 * v + 3]);
-              w.z = pack2<F16>(o[8 * v + 4], o[8 * v + 5]);
-              w.w = pack2<F16>(o[8 * v + 6], o[8 * v + 7]);
+              w.x = pack2<F16>(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+              w.y = pack2<F16>(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+              w.z = pack2<F16>(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+              w.w = pack2<F16>(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
               orow[c / 8 + v] = w;
             }
           }
         }
-        if (t == 0 && live)
-          p.lse[(size_t)bh * p.N + grow] = (m + log2f(L)) * 0.69314718055994530942f;
+        // LSE: dense [B*Hq, N], packed [Hq, total]
+        const size_t lse_idx =
+            VARLEN ? (size_t)U.h * p.total + U.seq0 + grow : (size_t)U.bh * p.N + grow;
+        if (live) p.lse[lse_idx] = (m_used + log2f(l)) * 0.69314718055994530942f;
       }
-    }
-    if (!KVSPLIT && ok && n_t > 0) ok = __all_sync(0xffffffffu, mbar_wait_inl(bar_o(), 0, wc));
-    if (!KVSPLIT && ok && n_t > 0) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      const bool live = grow < N;
-      // row grow of the output: dense [B*Hq, N, D], or packed [total, Hq, D]
-      const size_t orow_idx = VARLEN ? ((size_t)(seq0 + (live ? grow : 0)) * p.Hq + h)
-                                     : ((size_t)bh * p.N + (size_t)(live ? grow : 0));
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * D);
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tO + c, r);
-        tmem_ld_wait();
-        if (live) {
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack2<F16>(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-            w.y = pack2<F16>(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-            w.z = pack2<F16>(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-            w.w = pack2<F16>(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-            orow[c / 8 + v] = w;
+      // This warp has read O out of TMEM: the next unit's first P.V may
+      // overwrite it (KVSPLIT: both accumulators, read by both warpgroups).
+      if (ok) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (KVSPLIT) {
+            mbar_arrive(bar_of(0));
+            mbar_arrive(bar_of(1));
+          } else {
+            mbar_arrive(bar_of(t));
           }
         }
       }
-      // LSE: dense [B*Hq, N], packed [Hq, total]
-      const size_t lse_idx = VARLEN ? (size_t)h * p.total + seq0 + grow : (size_t)bh * p.N + grow;
-      if (live) p.lse[lse_idx] = (m_used + log2f(l)) * 0.69314718055994530942f;
     }
   }
 

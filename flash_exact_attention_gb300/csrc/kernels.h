@@ -19,6 +19,7 @@ struct FwdParams {
   float scale_log2;     // scale * log2(e)
   uint64_t timeout_ns;  // limit of every device-side wait
   unsigned int* err;    // device error word
+  int ctas;             // persistent CTAs of the dense forward (0: one CTA per work unit)
   // Stieltjes forward only (lse then holds the pole): the softmax scale and
   // the number of Newton steps.
   float scale;
