@@ -482,7 +482,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const float* delta = lse2 + 128;
       const bool diag = CAUSAL && q_tile(it) == j;
       float pf[64];
-      {
+      // The masks (causal: query < key on the diagonal tile; ragged: key rows
+      // past N) apply to few tiles; the others take a copy of the loop without
+      // them (a warp-uniform choice), which saves issue slots on every pair.
+      auto p_phase = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value != 0;
         uint32_t sr[2][16];
         tmem_ld16(ts, sr[0]);
 #pragma unroll
@@ -503,12 +507,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                   make_float2(__uint_as_float(sr[bb][ee]), __uint_as_float(sr[bb][ee + 1])), c2,
                   nl);
               float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              if (diag) {  // causal: query < key is masked
-                const int q = ch * 64 + qc + 2 * h;
-                if (q < row) pp.x = 0.f;
-                if (q + 1 < row) pp.y = 0.f;
+              if constexpr (kMasked) {
+                if (diag) {  // causal: query < key is masked
+                  const int q = ch * 64 + qc + 2 * h;
+                  if (q < row) pp.x = 0.f;
+                  if (q + 1 < row) pp.y = 0.f;
+                }
+                if (!key_live) pp = make_float2(0.f, 0.f);
               }
-              if (!key_live) pp = make_float2(0.f, 0.f);
               pf[c * 16 + ee] = pp.x;
               pf[c * 16 + ee + 1] = pp.y;
               pk[ee / 2] = pack2<F16>(pp.x, pp.y);
@@ -517,7 +523,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           // P^T (bf16) over S^T columns this warp has already read.
           tmem_st8(ts + c * 8, pk);
         }
-      }
+      };
+      if (__any_sync(0xffffffffu, diag || !key_live))
+        p_phase(IntConst<1>{});
+      else
+        p_phase(IntConst<0>{});
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
