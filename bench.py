@@ -111,14 +111,14 @@ FAMILY_SOURCES = {
 }
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
 # Kernel instantiations that only one of the widened rows launches (template
-# arguments as ncu prints them, spaces removed): their DRAM figures are
-# recorded under that row's name whatever --workload says.
+# arguments as ncu prints them, spaces removed, booleans as 0/1): their DRAM
+# figures are recorded under that row's name whatever --workload says.
 NEXT_ROW_KERNELS = {
-    "stj_kernel<128,false,4>": "stieltjes_b2_h16_n8192_d128_q4",
-    "fwd_kernel<128,true,false,true,false>": "varlen_causal_gqa_32seq_d128",
-    "bwd_kernel<128,true,false,true,true>": "varlen_bwd_causal_gqa_32seq_d128",
-    "bwd_kernel<128,false,false,false,false>": "bwd_deterministic_b2_h16_n8192_d128",
-    "bwd_dq_kernel<128,false,false>": "bwd_deterministic_b2_h16_n8192_d128",
+    "stj_kernel<128,0,4>": "stieltjes_b2_h16_n8192_d128_q4",
+    "fwd_kernel<128,1,0,1,0,0>": "varlen_causal_gqa_32seq_d128",
+    "bwd_kernel<128,1,0,1,1>": "varlen_bwd_causal_gqa_32seq_d128",
+    "bwd_kernel<128,0,0,0,0>": "bwd_deterministic_b2_h16_n8192_d128",
+    "bwd_dq_kernel<128,0,0>": "bwd_deterministic_b2_h16_n8192_d128",
 }
 
 
@@ -162,15 +162,18 @@ def _traffic_or_why(family, workload, second_family=None):
 
 
 def _ncu_kernel_key(name):
-    """'void attn::fwd_kernel<128, false, ...>(...)' -> ('fwd_kernel',
-    'fwd_kernel<128,false,...>')."""
-    m = re.search(r"attn::(\w+)<([^>]*)>", name)
+    """'void fwd_kernel<128, 0, 0, 0, 0, 0>(...)' (ncu's form; also with an
+    attn:: prefix, true/false or (bool)1/(bool)0) -> ('fwd_kernel',
+    'fwd_kernel<128,0,0,0,0,0>')."""
+    m = re.search(r"(?:void\s+)?(?:attn::)?(\w+)<([^>]*)>", name)
     if not m:
-        m2 = re.search(r"attn::(\w+)", name)
+        m2 = re.search(r"(?:void\s+)?(?:attn::)?(\w+)", name)
         fam = m2.group(1) if m2 else name.strip()
         return fam, fam
-    args = m.group(2).replace(" ", "").replace("(bool)0", "false").replace("(bool)1", "true")
-    return m.group(1), "%s<%s>" % (m.group(1), args)
+    args = [a.strip() for a in m.group(2).split(",")]
+    norm = {"true": "1", "false": "0", "(bool)1": "1", "(bool)0": "0"}
+    args = [norm.get(a, a) for a in args]
+    return m.group(1), "%s<%s>" % (m.group(1), ",".join(args))
 
 
 def record_traffic(csv_path, workload, command):
@@ -761,8 +764,11 @@ def _time_ms(torch, fn, warm=3, reps=10):
     return e0.elapsed_time(e1) / reps
 
 
-def next_rows(seed):
-    """The widened rows, each timed on its own page's workload (synthetic
+NEXT_ROW_GROUPS = ("nystrom", "stieltjes", "varlen", "deterministic")
+
+
+def next_rows(seed, only=NEXT_ROW_GROUPS):
+    """The widened rows (the groups in `only`), each timed on its own page's workload (synthetic
     inputs of that shape), outside the headline step's timed region:
       - Nystrom forward, bound by HBM: algorithmic bytes are Q twice (landmark
         pooling, output pass), K, V and O once;
@@ -786,8 +792,9 @@ def next_rows(seed):
         return {n: to_torch_bf16(a).to("cuda") for n, a in x.items()}
 
     # Nystrom: the page's high batch x head shape and its long-context shape.
-    for name, (B, H, N, D, m) in (("nystrom_b4_h16_n131072_d128_m64", (4, 16, 131072, 128, 64)),
-                                  ("nystrom_b1_h4_n2097152_d64_m32", (1, 4, 2097152, 64, 32))):
+    nys_shapes = (("nystrom_b4_h16_n131072_d128_m64", (4, 16, 131072, 128, 64)),
+                  ("nystrom_b1_h4_n2097152_d64_m32", (1, 4, 2097152, 64, 32)))
+    for name, (B, H, N, D, m) in (nys_shapes if "nystrom" in only else ()):
         g = torch.Generator(device="cuda").manual_seed(seed)
         q, k, v = (torch.randn(B, H, N, D, device="cuda", generator=g).to(torch.bfloat16)
                    for _ in range(3))
@@ -814,90 +821,93 @@ def next_rows(seed):
 
     # Stieltjes attention, order 4, the page's three Newton steps.
     B, H, N, D = 2, 16, 8192, 128
-    t = dev_inputs(B, H, H, N, D)
-    ms = _time_ms(torch, lambda: binding.stieltjes_attn(t["q"], t["k"], t["v"], order=4,
-                                                        newton_steps=3))
-    st = binding.attn_device_status()
-    if st:
-        raise binding.AttnError(st, "stieltjes")
-    att = 4.0 * B * H * N * N * D / ms / 1e9
-    tensor = att / 2 * (3 + 2 + 1)
-    rows["stieltjes_b2_h16_n8192_d128_q4"] = {
-        "workload": "Stieltjes forward B=2 H=16 N=8192 D=128, order 4, 3 Newton steps",
-        "metric": "attention TFLOPS (4 B H N^2 D per call)", "value": round(att, 1),
-        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
-        "roofline": {"bound": "tensor", "achieved": round(tensor, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tensor / peak_burst, 4),
-                     **_traffic_or_why("stj_kernel", "stieltjes_b2_h16_n8192_d128_q4"),
-                     "algorithmic_flops_per_launch": 2.0 * B * H * N * N * D * 6,
-                     "peak_source": "%s bf16 burst" % peak_src}}
+    if "stieltjes" in only:
+        t = dev_inputs(B, H, H, N, D)
+        ms = _time_ms(torch, lambda: binding.stieltjes_attn(t["q"], t["k"], t["v"], order=4,
+                                                            newton_steps=3))
+        st = binding.attn_device_status()
+        if st:
+            raise binding.AttnError(st, "stieltjes")
+        att = 4.0 * B * H * N * N * D / ms / 1e9
+        tensor = att / 2 * (3 + 2 + 1)
+        rows["stieltjes_b2_h16_n8192_d128_q4"] = {
+            "workload": "Stieltjes forward B=2 H=16 N=8192 D=128, order 4, 3 Newton steps",
+            "metric": "attention TFLOPS (4 B H N^2 D per call)", "value": round(att, 1),
+            "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
+            "roofline": {"bound": "tensor", "achieved": round(tensor, 1), "peak": peak_burst,
+                         "unit": "TFLOP/s", "frac": round(tensor / peak_burst, 4),
+                         **_traffic_or_why("stj_kernel", "stieltjes_b2_h16_n8192_d128_q4"),
+                         "algorithmic_flops_per_launch": 2.0 * B * H * N * N * D * 6,
+                         "peak_source": "%s bf16 burst" % peak_src}}
 
-    # Ragged batch, packed without padding: causal GQA (Hq 16, Hkv 4, D 128),
-    # 32 sequences of seeded lengths 1..8192 (about 130 k tokens).
-    import numpy as np
-    Hq, Hkv, D = 16, 4, 128
-    lens = np.random.default_rng(seed).integers(1, 8193, size=32)
-    total, ms_max = int(lens.sum()), int(lens.max())
-    g = torch.Generator(device="cuda").manual_seed(seed)
-    q = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
-    k = torch.randn(total, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
-    v = torch.randn(total, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
-    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device="cuda")
-    ms = _time_ms(torch, lambda: binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True))
-    st = binding.attn_device_status()
-    if st:
-        raise binding.AttnError(st, "varlen forward")
-    flops = sum(4.0 * Hq * float(n) * float(n) * D / 2 for n in lens)
-    tf = flops / ms / 1e9
-    rows["varlen_causal_gqa_32seq_d128"] = {
-        "workload": "packed ragged batch, causal GQA Hq=16 Hkv=4 D=128, 32 sequences of "
-                    "seeded lengths 1..8192 (%d tokens, longest %d)" % (total, ms_max),
-        "metric": "forward TFLOPS (sum over sequences of 2 Hq n^2 D)", "value": round(tf, 1),
-        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
-        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
-                     **_traffic_or_why("fwd_kernel", "varlen_causal_gqa_32seq_d128"),
-                     "peak_source": "%s bf16 burst" % peak_src}}
-    o, lse = binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True)
-    do = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
-    ms = _time_ms(torch, lambda: binding.flash_attn_varlen_bwd(q, k, v, o, lse, do, cu, ms_max,
-                                                               causal=True))
-    st = binding.attn_device_status()
-    if st:
-        raise binding.AttnError(st, "varlen backward")
-    tf = 2.5 * flops / ms / 1e9
-    rows["varlen_bwd_causal_gqa_32seq_d128"] = {
-        "workload": "backward of the same packed ragged batch (%d tokens)" % total,
-        "metric": "backward TFLOPS (2.5x the forward's FLOPs)", "value": round(tf, 1),
-        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4),
-        "launches": 3, "timed_as": "whole attn_bwd_varlen call (memset + 3 kernels)",
-        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
-                     **_traffic_or_why("bwd_kernel", "varlen_bwd_causal_gqa_32seq_d128"),
-                     "peak_source": "%s bf16 burst" % peak_src}}
-    del q, k, v, cu, o, lse, do
-    torch.cuda.empty_cache()
+    if "varlen" in only:
+        # Ragged batch, packed without padding: causal GQA (Hq 16, Hkv 4, D 128),
+        # 32 sequences of seeded lengths 1..8192 (about 130 k tokens).
+        import numpy as np
+        Hq, Hkv, D = 16, 4, 128
+        lens = np.random.default_rng(seed).integers(1, 8193, size=32)
+        total, ms_max = int(lens.sum()), int(lens.max())
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        q = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
+        k = torch.randn(total, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
+        v = torch.randn(total, Hkv, D, device="cuda", generator=g).to(torch.bfloat16)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), device="cuda")
+        ms = _time_ms(torch, lambda: binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True))
+        st = binding.attn_device_status()
+        if st:
+            raise binding.AttnError(st, "varlen forward")
+        flops = sum(4.0 * Hq * float(n) * float(n) * D / 2 for n in lens)
+        tf = flops / ms / 1e9
+        rows["varlen_causal_gqa_32seq_d128"] = {
+            "workload": "packed ragged batch, causal GQA Hq=16 Hkv=4 D=128, 32 sequences of "
+                        "seeded lengths 1..8192 (%d tokens, longest %d)" % (total, ms_max),
+            "metric": "forward TFLOPS (sum over sequences of 2 Hq n^2 D)", "value": round(tf, 1),
+            "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 1,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
+                         "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                         **_traffic_or_why("fwd_kernel", "varlen_causal_gqa_32seq_d128"),
+                         "peak_source": "%s bf16 burst" % peak_src}}
+        o, lse = binding.flash_attn_varlen(q, k, v, cu, ms_max, causal=True)
+        do = torch.randn(total, Hq, D, device="cuda", generator=g).to(torch.bfloat16)
+        ms = _time_ms(torch, lambda: binding.flash_attn_varlen_bwd(q, k, v, o, lse, do, cu, ms_max,
+                                                                   causal=True))
+        st = binding.attn_device_status()
+        if st:
+            raise binding.AttnError(st, "varlen backward")
+        tf = 2.5 * flops / ms / 1e9
+        rows["varlen_bwd_causal_gqa_32seq_d128"] = {
+            "workload": "backward of the same packed ragged batch (%d tokens)" % total,
+            "metric": "backward TFLOPS (2.5x the forward's FLOPs)", "value": round(tf, 1),
+            "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4),
+            "launches": 3, "timed_as": "whole attn_bwd_varlen call (memset + 3 kernels)",
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
+                         "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                         **_traffic_or_why("bwd_kernel", "varlen_bwd_causal_gqa_32seq_d128"),
+                         "peak_source": "%s bf16 burst" % peak_src}}
+        del q, k, v, cu, o, lse, do
+        torch.cuda.empty_cache()
 
-    # Deterministic backward on the headline shape.
-    t = dev_inputs(B, H, H, N, D, with_do=True)
-    o, lse = binding.flash_attn(t["q"], t["k"], t["v"])
-    ms = _time_ms(torch, lambda: binding.flash_attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"],
-                                                        deterministic=True))
-    st = binding.attn_device_status()
-    if st:
-        raise binding.AttnError(st, "deterministic backward")
-    tf = 2.5 * 4.0 * B * H * N * N * D / ms / 1e9
-    rows["bwd_deterministic_b2_h16_n8192_d128"] = {
-        "workload": "deterministic backward B=2 H=16 N=8192 D=128 non-causal",
-        "metric": "backward TFLOPS (2.5x forward FLOPs)", "value": round(tf, 1),
-        "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 3,
-        "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
-                     "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
-                     **_traffic_or_why("bwd_kernel", "bwd_deterministic_b2_h16_n8192_d128",
-                                       "bwd_dq_kernel"),
-                     "peak_source": "%s bf16 burst" % peak_src}}
-    del t, o, lse
-    torch.cuda.empty_cache()
+    if "deterministic" in only:
+        # Deterministic backward on the headline shape.
+        t = dev_inputs(B, H, H, N, D, with_do=True)
+        o, lse = binding.flash_attn(t["q"], t["k"], t["v"])
+        ms = _time_ms(torch, lambda: binding.flash_attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"],
+                                                            deterministic=True))
+        st = binding.attn_device_status()
+        if st:
+            raise binding.AttnError(st, "deterministic backward")
+        tf = 2.5 * 4.0 * B * H * N * N * D / ms / 1e9
+        rows["bwd_deterministic_b2_h16_n8192_d128"] = {
+            "workload": "deterministic backward B=2 H=16 N=8192 D=128 non-causal",
+            "metric": "backward TFLOPS (2.5x forward FLOPs)", "value": round(tf, 1),
+            "unit": "TFLOPS", "higher_is_better": True, "ms": round(ms, 4), "launches": 3,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak_burst,
+                         "unit": "TFLOP/s", "frac": round(tf / peak_burst, 4),
+                         **_traffic_or_why("bwd_kernel", "bwd_deterministic_b2_h16_n8192_d128",
+                                           "bwd_dq_kernel"),
+                         "peak_source": "%s bf16 burst" % peak_src}}
+        del t, o, lse
+        torch.cuda.empty_cache()
     return rows
 
 
@@ -1036,15 +1046,32 @@ def main():
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the widened rows (Nystrom, Stieltjes, varlen, deterministic "
                          "backward)")
+    ap.add_argument("--next-rows-only", metavar="GROUPS",
+                    help="time only these widened rows (comma list of %s) and print them; "
+                         "for profiling them alone" % ",".join(NEXT_ROW_GROUPS))
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="record the DRAM bytes per launch of an ncu --csv capture (metrics "
                          "dram__bytes_read.sum, dram__bytes_write.sum) taken on --workload "
                          "into profiles/dram_traffic.json, then exit")
     ap.add_argument("--record-command", default="",
                     help="the ncu command line the capture came from (stored beside it)")
+    ap.add_argument("--traffic-json", default=None,
+                    help="file the records go to (default profiles/dram_traffic.json)")
     args = ap.parse_args()
     if args.record_traffic:
+        global TRAFFIC_JSON
+        if args.traffic_json:
+            TRAFFIC_JSON = args.traffic_json
         record_traffic(args.record_traffic, args.workload, args.record_command)
+        return
+    if args.next_rows_only:
+        groups = tuple(g for g in args.next_rows_only.split(",") if g)
+        bad = [g for g in groups if g not in NEXT_ROW_GROUPS]
+        if bad:
+            ap.error("unknown row groups: %s" % ",".join(bad))
+        import torch
+        torch.cuda.set_device(_dist_env()[2])
+        print(json.dumps({"next_rows": next_rows(args.seed, groups)}), flush=True)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -9,12 +9,14 @@ import bench
 
 def test_ncu_kernel_key_normalises_template_arguments():
     fam, key = bench._ncu_kernel_key(
-        "void attn::fwd_kernel<128, false, false, false, false>(CUtensorMap, CUtensorMap, "
-        "CUtensorMap, attn::FwdParams)")
-    assert (fam, key) == ("fwd_kernel", "fwd_kernel<128,false,false,false,false>")
-    fam, key = bench._ncu_kernel_key("void attn::bwd_kernel<64, (bool)1, (bool)0, (bool)1, "
-                                     "(bool)0>(CUtensorMap)")
-    assert key == "bwd_kernel<64,true,false,true,false>"
+        "void fwd_kernel<128, 0, 0, 0, 0, 0>(CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, "
+        "FwdParams)")
+    assert (fam, key) == ("fwd_kernel", "fwd_kernel<128,0,0,0,0,0>")
+    fam, key = bench._ncu_kernel_key("void attn::bwd_kernel<64, (bool)1, (bool)0, true, "
+                                     "false>(CUtensorMap)")
+    assert key == "bwd_kernel<64,1,0,1,0>"
+    assert bench._ncu_kernel_key("void stj_kernel<128, 0, 4>(CUtensorMap_st)")[1] == \
+        "stj_kernel<128,0,4>"
     assert bench._ncu_kernel_key("void attn::nys_pool_kernel(attn::NysParams)")[0] == \
         "nys_pool_kernel"
 
@@ -34,8 +36,8 @@ def _csv(rows):
 def test_record_traffic_writes_json_that_the_bench_reads(tmp_path, monkeypatch):
     out = tmp_path / "dram_traffic.json"
     monkeypatch.setattr(bench, "TRAFFIC_JSON", str(out))
-    fwd = "void attn::fwd_kernel<128, false, false, false, false>(CUtensorMap)"
-    stj = "void attn::stj_kernel<128, false, 4>(CUtensorMap)"
+    fwd = "void fwd_kernel<128, 0, 0, 0, 0, 0>(CUtensorMap_st)"
+    stj = "void stj_kernel<128, 0, 4>(CUtensorMap_st)"
     rows = []
     for lid, (rd, wr) in enumerate([(200.0, 45.0), (210.0, 45.0), (190.0, 45.0)]):
         rows += [(lid, fwd, "dram__bytes_read.sum", "Mbyte", "%.1f" % rd),
