@@ -8,7 +8,8 @@
 // Three kernels per call:
 //   bwd_preprocess  Delta_i = sum_d dO_id O_id and LSE2_i = LSE_i log2(e), written
 //                   to row-padded buffers (rows past N: LSE2 = +inf so P = 0,
-//                   Delta = 0); zeroes the fp32 dQ accumulator.
+//                   Delta = 0); zeroes the fp32 dQ accumulator.  Memory-bound:
+//                   16-byte loads, several rows per warp in flight.
 //   bwd_kernel      one CTA per (batch, kv head, 128-key tile j).  It loops over
 //                   the query heads of its group and over the query tiles i
 //                   (i >= j when causal: tiles above the diagonal are skipped):
@@ -16,12 +17,13 @@
 //                     dP^T = V_j dO_i^T           (tcgen05, TMEM)
 //                     P^T  = 2^(S^T c - LSE2_i), dS^T = P^T o (dP^T - Delta_i)
 //                     dV_j += P^T dO_i            (A = P^T from TMEM)
-//                     dQ_i  = dS K_j              (A = the dS^T tile read MN-major)
-//                     dK_j += dS^T Q_i            (A = dS^T from shared memory)
+//                     dK_j += dS^T Q_i            (A = dS^T from TMEM)
+//                     dQ_i  = dS K_j              (A = the dS^T tile in shared
+//                                                  memory, read MN-major)
 //                   dK/dV stay in TMEM across the whole group (no GQA reduction
 //                   pass).  The tensor cores run, per query tile i,
-//                     dP_i, dV_i, S_{i+1}, dQ_i, dK_i
-//                   so that P_{i+1} is computed while dQ_i, dK_i and dP_{i+1}
+//                     dP_i, dV_i, S_{i+1}, dK_i, dQ_i
+//                   so that P_{i+1} is computed while dK_i, dQ_i and dP_{i+1}
 //                   run, and dS_i while dV_i and S_{i+1} run.  dQ_i goes TMEM ->
 //                   registers of a dedicated warpgroup (freeing the columns for
 //                   dP_{i+1} at once) -> a two-slot shared staging ring -> TMA
@@ -642,8 +644,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-// Delta and LSE2 into row-padded buffers; zero the dQ accumulator.  One warp per
-// padded row (b*Hq + h, i), i < Npad.
+// Rows of the preprocessing kernel per CTA: D/8 lanes per padded row (16
+// bytes of O and of dO each), 32*8/D rows per warp and pass, kPrePasses
+// passes with all loads issued before the first reduction (several KB in
+// flight per warp: one 128-byte row per warp left the kernel latency-bound
+// at a third of the copy bandwidth).
+constexpr int kPrePasses = 4;
+template <int D>
+constexpr int pre_rows_per_cta() { return 8 * (32 * 8 / D) * kPrePasses; }
+
+// dO . O of one row from its D/8 lanes (8 elements each, lane l the elements
+// [8l, 8l+8)), summed over those lanes; both preprocessing kernels use it, so
+// a packed batch of equal lengths gets the dense batch's Delta bit for bit.
+template <int D, bool F16>
+__device__ __forceinline__ float pre_row_dot(const uint4& a, const uint4& g) {
+  auto dot2 = [](uint32_t u, uint32_t v) {
+    const float2 x = unpack2<F16>(u), y = unpack2<F16>(v);
+    return x.x * y.x + x.y * y.y;
+  };
+  float acc = dot2(a.x, g.x) + dot2(a.y, g.y) + dot2(a.z, g.z) + dot2(a.w, g.w);
+#pragma unroll
+  for (int off = D / 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  return acc;
+}
+
+// Delta and LSE2 into row-padded buffers; zero the dQ accumulator (and, with
+// the group split, the dK/dV accumulators).  Padded row r = (b*Hq + h, i),
+// i < Npad; rows past N get LSE2 = +inf, Delta = 0.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
@@ -651,45 +678,52 @@ __global__ void __launch_bounds__(256)
                    float* __restrict__ delta, float* __restrict__ dq_acc, long long rows, int N,
                    int Npad, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
                    long long kv_rows) {
-  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int L = D / 8;       // lanes per row
+  constexpr int RPW = 32 / L;    // rows per warp and pass
+  static_assert(128 % (RPW * kPrePasses) == 0, "a warp's rows lie in one (batch, head)");
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const long long bh = r / Npad;
-  const int i = (int)(r % Npad);
-  float acc = 0.f;
-  if (i < N) {
-    constexpr int kPer = D / 32;  // elements per lane: 2 or 4
-    const size_t base = ((size_t)bh * N + i) * D + (size_t)lane * kPer;
-    if (kPer == 2) {
-      const float2 a = unpack2<F16>(*reinterpret_cast<const uint32_t*>(o + base));
-      const float2 g = unpack2<F16>(*reinterpret_cast<const uint32_t*>(dout + base));
-      acc = a.x * g.x + a.y * g.y;
-    } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-      const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
-      const float2 a0 = unpack2<F16>(a.x), a1 = unpack2<F16>(a.y);
-      const float2 g0 = unpack2<F16>(g.x), g1 = unpack2<F16>(g.y);
-      acc = a0.x * g0.x + a0.y * g0.y + a1.x * g1.x + a1.y * g1.y;
+  const int sub = lane / L, l = lane % L;
+  // The warp's rows: RPW * kPrePasses consecutive padded rows of one (batch,
+  // head) plane (Npad is a multiple of 128).
+  const long long rw = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (RPW * kPrePasses);
+  const long long bh = rw / Npad;
+  const int iw = (int)(rw - bh * Npad);
+  uint4 a[kPrePasses], g[kPrePasses];
+#pragma unroll
+  for (int ps = 0; ps < kPrePasses; ++ps) {
+    const int i = iw + ps * RPW + sub;
+    a[ps] = make_uint4(0u, 0u, 0u, 0u);
+    g[ps] = make_uint4(0u, 0u, 0u, 0u);
+    if (rw < rows && i < N) {
+      const size_t base = ((size_t)bh * N + i) * D + (size_t)l * 8;
+      a[ps] = *reinterpret_cast<const uint4*>(o + base);
+      g[ps] = *reinterpret_cast<const uint4*>(dout + base);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   }
-  if (lane == 0) {
-    lse2[r] = i < N ? lse[(size_t)bh * N + i] * 1.4426950408889634f : INFINITY;
-    delta[r] = acc;
-  }
-  if (dq_acc != nullptr) {  // none in the deterministic backward
-    float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)r * D);
 #pragma unroll
-    for (int t = lane; t < D / 4; t += 32) z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (r < kv_rows) {  // group split: zero the dK/dV accumulators too
-    float4* zk = reinterpret_cast<float4*>(dk_acc + (size_t)r * D);
-    float4* zv = reinterpret_cast<float4*>(dv_acc + (size_t)r * D);
-#pragma unroll
-    for (int t = lane; t < D / 4; t += 32) {
-      zk[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-      zv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int ps = 0; ps < kPrePasses; ++ps) {
+    const float acc = pre_row_dot<D, F16>(a[ps], g[ps]);
+    if (rw >= rows) continue;
+    const int i = iw + ps * RPW + sub;
+    const long long r = rw + ps * RPW + sub;
+    if (l == 0) {
+      lse2[r] = i < N ? lse[(size_t)bh * N + i] * 1.4426950408889634f : INFINITY;
+      delta[r] = acc;
+    }
+    // D fp32 per accumulator row: two 16-byte stores per lane
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dq_acc != nullptr) {  // none in the deterministic backward
+      float4* zq = reinterpret_cast<float4*>(dq_acc + (size_t)r * D) + 2 * l;
+      zq[0] = z;
+      zq[1] = z;
+    }
+    if (r < kv_rows) {  // group split: zero the dK/dV accumulators too
+      float4* zk = reinterpret_cast<float4*>(dk_acc + (size_t)r * D) + 2 * l;
+      float4* zv = reinterpret_cast<float4*>(dv_acc + (size_t)r * D) + 2 * l;
+      zk[0] = z;
+      zk[1] = z;
+      zv[0] = z;
+      zv[1] = z;
     }
   }
 }
@@ -698,44 +732,47 @@ __global__ void __launch_bounds__(256)
 // i < Npad, from token cu_seqlens[b] + i of o/dout [total, Hq, D] and lse
 // [Hq, total]; rows past the sequence's end (or of a sequence whose offsets
 // are not valid, which the main kernel reports) get LSE2 = +inf, Delta = 0.
-// One warp per padded row.
+// The lane and row layout of bwd_preprocess.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_varlen(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                           const float* __restrict__ lse, const int* __restrict__ cu_seqlens,
                           float* __restrict__ lse2, float* __restrict__ delta, long long rows,
                           int Hq, int Npad, int max_seqlen, int total) {
-  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int L = D / 8;       // lanes per row
+  constexpr int RPW = 32 / L;    // rows per warp and pass
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const long long bh = r / Npad;
-  const int i = (int)(r % Npad);
+  const int sub = lane / L, l = lane % L;
+  const long long rw = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (RPW * kPrePasses);
+  if (rw >= rows) return;
+  const long long bh = rw / Npad;  // the warp's rows share one (sequence, head)
+  const int iw = (int)(rw - bh * Npad);
   const int b = (int)(bh / Hq), h = (int)(bh % Hq);
   const int seq0 = cu_seqlens[b];
   const int len = cu_seqlens[b + 1] - seq0;
   const bool valid = seq0 >= 0 && len >= 0 && len <= max_seqlen && seq0 <= total - len;
-  const bool live = valid && i < len;
-  float acc = 0.f;
-  if (live) {
-    constexpr int kPer = D / 32;
-    const size_t base = ((size_t)(seq0 + i) * Hq + h) * D + (size_t)lane * kPer;
-    if (kPer == 2) {
-      const float2 a = unpack2<F16>(*reinterpret_cast<const uint32_t*>(o + base));
-      const float2 g = unpack2<F16>(*reinterpret_cast<const uint32_t*>(dout + base));
-      acc = a.x * g.x + a.y * g.y;
-    } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-      const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
-      const float2 a0 = unpack2<F16>(a.x), a1 = unpack2<F16>(a.y);
-      const float2 g0 = unpack2<F16>(g.x), g1 = unpack2<F16>(g.y);
-      acc = a0.x * g0.x + a0.y * g0.y + a1.x * g1.x + a1.y * g1.y;
-    }
+  uint4 a[kPrePasses], g[kPrePasses];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  for (int ps = 0; ps < kPrePasses; ++ps) {
+    const int i = iw + ps * RPW + sub;
+    a[ps] = make_uint4(0u, 0u, 0u, 0u);
+    g[ps] = make_uint4(0u, 0u, 0u, 0u);
+    if (valid && i < len) {
+      const size_t base = ((size_t)(seq0 + i) * Hq + h) * D + (size_t)l * 8;
+      a[ps] = *reinterpret_cast<const uint4*>(o + base);
+      g[ps] = *reinterpret_cast<const uint4*>(dout + base);
+    }
   }
-  if (lane == 0) {
-    lse2[r] = live ? lse[(size_t)h * total + seq0 + i] * 1.4426950408889634f : INFINITY;
-    delta[r] = acc;
+#pragma unroll
+  for (int ps = 0; ps < kPrePasses; ++ps) {
+    const float acc = pre_row_dot<D, F16>(a[ps], g[ps]);
+    const int i = iw + ps * RPW + sub;
+    const bool live = valid && i < len;
+    if (l == 0) {
+      const long long r = rw + ps * RPW + sub;
+      lse2[r] = live ? lse[(size_t)h * total + seq0 + i] * 1.4426950408889634f : INFINITY;
+      delta[r] = live ? acc : 0.f;
+    }
   }
 }
 

@@ -24,7 +24,8 @@ cudaError_t launch_bwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     return cudaErrorInvalidValue;
   const long long prow = (long long)p.B * p.Hq * p.Npad;  // padded rows
   const long long kv_rows = split ? (long long)p.B * p.Hkv * p.Npad : 0;
-  bwd_preprocess<D, F16><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
+  constexpr long long kPreRows = pre_rows_per_cta<D>();
+  bwd_preprocess<D, F16><<<(unsigned)((prow + kPreRows - 1) / kPreRows), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse,
       const_cast<float*>(p.lse2), const_cast<float*>(p.delta), p.dq_acc, prow, p.N, p.Npad,
       p.dk_acc, p.dv_acc, kv_rows);
@@ -77,7 +78,9 @@ cudaError_t launch_bwd_varlen_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, (size_t)qrows * D * 4, stream);
   if (e != cudaSuccess) return e;
   const long long prow = (long long)p.B * p.Hq * p.Npad;
-  bwd_preprocess_varlen<D, F16><<<(unsigned)((prow + 7) / 8), 256, 0, stream>>>(
+  constexpr long long kPreRows = pre_rows_per_cta<D>();
+  bwd_preprocess_varlen<D, F16><<<(unsigned)((prow + kPreRows - 1) / kPreRows), 256, 0,
+                                  stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, p.cu_seqlens,
       const_cast<float*>(p.lse2), const_cast<float*>(p.delta), prow, p.Hq, p.Npad, p.N, p.total);
   e = cudaGetLastError();
