@@ -133,70 +133,91 @@ __global__ void __launch_bounds__(D) nys_qt_kernel(const NysParams p) {
 }
 
 // ============================================================ 5: landmarks, pinv, Y
-// C (MR x NC) = A B with A given as its transpose At (At[k][i] = A[i][k], row
-// stride lda) and B (row stride ldb), K-step k reading TR values of At and TC
-// of B along their contiguous index (vector loads for 2 and 4) for TR x TC
-// multiply-adds held in registers; each thread owns TR x TC blocks of C
-// (grid-stride over the CTA).  store(i, j, value) writes the result.
-template <int N>
-__device__ __forceinline__ void load_vec(const float* src, float (&v)[N]) {
-  if constexpr (N == 4) {
-    const float4 x = *reinterpret_cast<const float4*>(src);
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-  } else if constexpr (N == 2) {
-    const float2 x = *reinterpret_cast<const float2*>(src);
-    v[0] = x.x; v[1] = x.y;
-  } else {
+// C (MR x NC, both multiples of 16) = A B with A given as its transpose At
+// (At[k][i] = A[i][k], row stride lda) and B (row stride ldb), every entry
+// summed over k in order.  Each warp takes (8 TRL) x 16 blocks of C
+// (grid-stride over the CTA's warps); lane (rg, cg) = (lane / 4, lane % 4)
+// holds the TRL x 4 entries at rows TRL rg .. TRL rg + TRL - 1 and columns
+// 4 cg .. 4 cg + 3 of the block, and per K-step reads TRL values of At's row k
+// and 4 of B's with vector loads and issues 2 TRL packed fp32x2
+// multiply-adds.  These products are bound by shared-memory wavefronts: a
+// warp's vector load costs one wavefront per 32 floats it delivers, broadcast
+// or not, so larger register tiles (fewer loads per multiply-add) beat more
+// warps.  store(i, j, value) writes the result.
+template <int TRL, class Store>
+__device__ __forceinline__ void mm_blocks_t(const float* At, int lda, const float* B, int ldb, int K,
+                                            int MR, int NC, Store store) {
+  constexpr int BR = 8 * TRL;
+  const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+  const int nwarps = (int)(blockDim.x >> 5);
+  const int bcols = NC / 16, blocks = (MR / BR) * bcols;
+  const int ro = TRL * (lane >> 2), co = 4 * (lane & 3);
+  for (int blk = warp; blk < blocks; blk += nwarps) {
+    const int r0 = (blk / bcols) * BR + ro, c0 = (blk % bcols) * 16 + co;
+    const float* a = At + r0;
+    const float* bb = B + c0;
+    float2 acc[TRL][2];
 #pragma unroll
-    for (int a = 0; a < N; ++a) v[a] = src[a];
+    for (int x = 0; x < TRL; ++x) acc[x][0] = acc[x][1] = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+      float av[TRL];
+      if constexpr (TRL == 8) {
+        const float4 v4 = *reinterpret_cast<const float4*>(a + k * lda);
+        const float4 w4 = *reinterpret_cast<const float4*>(a + k * lda + 4);
+        av[0] = v4.x; av[1] = v4.y; av[2] = v4.z; av[3] = v4.w;
+        av[4] = w4.x; av[5] = w4.y; av[6] = w4.z; av[7] = w4.w;
+      } else if constexpr (TRL == 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(a + k * lda);
+        av[0] = v4.x; av[1] = v4.y; av[2] = v4.z; av[3] = v4.w;
+      } else {
+        const float2 v2 = *reinterpret_cast<const float2*>(a + k * lda);
+        av[0] = v2.x; av[1] = v2.y;
+      }
+      const float4 bv = *reinterpret_cast<const float4*>(bb + k * ldb);
+      const float2 b01 = make_float2(bv.x, bv.y), b23 = make_float2(bv.z, bv.w);
+#pragma unroll
+      for (int x = 0; x < TRL; ++x) {
+        const float2 ax = make_float2(av[x], av[x]);
+        acc[x][0] = __ffma2_rn(ax, b01, acc[x][0]);
+        acc[x][1] = __ffma2_rn(ax, b23, acc[x][1]);
+      }
+    }
+#pragma unroll
+    for (int x = 0; x < TRL; ++x) {
+      store(r0 + x, c0, acc[x][0].x);
+      store(r0 + x, c0 + 1, acc[x][0].y);
+      store(r0 + x, c0 + 2, acc[x][1].x);
+      store(r0 + x, c0 + 3, acc[x][1].y);
+    }
   }
 }
 
-template <int TR, int TC, class Store>
-__device__ __forceinline__ void mm_tiles(const float* At, int lda, const float* B, int ldb, int K,
-                                         int MR, int NC, Store store) {
-  const int tiles_c = NC / TC, tiles = (MR / TR) * tiles_c;
-  for (int tile = (int)threadIdx.x; tile < tiles; tile += (int)blockDim.x) {
-    const int r0 = (tile / tiles_c) * TR, c0 = (tile % tiles_c) * TC;
-    float acc[TR][TC];
-#pragma unroll
-    for (int a = 0; a < TR; ++a)
-#pragma unroll
-      for (int b = 0; b < TC; ++b) acc[a][b] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-      float av[TR], bv[TC];
-      load_vec<TR>(At + k * lda + r0, av);
-      load_vec<TC>(B + k * ldb + c0, bv);
-#pragma unroll
-      for (int a = 0; a < TR; ++a)
-#pragma unroll
-        for (int b = 0; b < TC; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < TR; ++a)
-#pragma unroll
-      for (int b = 0; b < TC; ++b) store(r0 + a, c0 + b, acc[a][b]);
-  }
+// The register tile for a shape: 8 x 4 for the 64 x 64 products over 64 steps
+// (4 warps; 12 wavefronts per 1024 multiply-adds), 4 x 4 where MR is a multiple
+// of 32, else 2 x 4.
+template <class Store>
+__device__ __forceinline__ void mm_blocks(const float* At, int lda, const float* B, int ldb, int K,
+                                          int MR, int NC, Store store) {
+  if (MR == 64 && NC == 64 && K <= 64)
+    mm_blocks_t<8>(At, lda, B, ldb, K, MR, NC, store);
+  else if (MR % 32 == 0)
+    mm_blocks_t<4>(At, lda, B, ldb, K, MR, NC, store);
+  else
+    mm_blocks_t<2>(At, lda, B, ldb, K, MR, NC, store);
 }
 
 // mp x mp result (mp in {16, 32, 48, 64}) over K steps into C (row stride mp);
 // ends with a __syncthreads.
 __device__ __forceinline__ void mm_sq(int mp, const float* At, int lda, const float* B, int ldb,
                                       int K, float* C) {
-  auto st = [&](int i, int j, float v) { C[i * mp + j] = v; };
-  switch (mp) {
-    case 16: mm_tiles<1, 1>(At, lda, B, ldb, K, 16, 16, st); break;
-    case 32: mm_tiles<1, 2>(At, lda, B, ldb, K, 32, 32, st); break;
-    case 48: mm_tiles<2, 3>(At, lda, B, ldb, K, 48, 48, st); break;
-    default: mm_tiles<4, 4>(At, lda, B, ldb, K, 64, 64, st); break;
-  }
+  mm_blocks(At, lda, B, ldb, K, mp, mp, [&](int i, int j, float v) { C[i * mp + j] = v; });
   __syncthreads();
 }
 
 // max over columns of the column |sums| times max over rows of the row |sums|
 // of an mp x mp matrix (zero padding does not change either); every thread
-// gets the result.  `red` holds 2 * 64 floats.  512 threads.
+// gets the result.  `red` holds 2 * 64 + 1 floats.  512 threads.
 __device__ __forceinline__ float norm1_norminf(const float* A, int mp, float* red) {
   const int t = (int)threadIdx.x, warp = t >> 5, lane = t & 31;
   if (t < mp) {
@@ -212,17 +233,38 @@ __device__ __forceinline__ float norm1_norminf(const float* A, int mp, float* re
     if (lane == 0) red[64 + r] = s;
   }
   __syncthreads();
-  float n1 = 0.f, ninf = 0.f;
-  for (int e = 0; e < mp; ++e) {
-    n1 = fmaxf(n1, red[e]);
-    ninf = fmaxf(ninf, red[64 + e]);
+  if (warp == 0) {  // the two maxima over (at most) 64 entries each
+    float n1 = 0.f, ninf = 0.f;
+    for (int e = lane; e < mp; e += 32) {
+      n1 = fmaxf(n1, red[e]);
+      ninf = fmaxf(ninf, red[64 + e]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n1 = fmaxf(n1, __shfl_xor_sync(0xffffffffu, n1, o));
+      ninf = fmaxf(ninf, __shfl_xor_sync(0xffffffffu, ninf, o));
+    }
+    if (lane == 0) red[128] = n1 * ninf;
   }
   __syncthreads();
-  return n1 * ninf;
+  const float r = red[128];
+  __syncthreads();
+  return r;
 }
 
-// Dst = Src^T for mp x mp matrices.
+// Dst = Src^T for mp x mp matrices.  At mp = 64 a warp moves 32 entries along
+// a diagonal, (i, j) = (32 h + lane, (c + lane) mod 64) for its piece (h, c),
+// so that both its reads (banks j mod 32) and its writes (banks i mod 32) hit
+// 32 different banks.
 __device__ __forceinline__ void smem_transpose(const float* src, float* dst, int mp) {
+  if (mp == 64) {
+    const int lane = (int)(threadIdx.x & 31);
+    for (int pc = (int)(threadIdx.x >> 5); pc < 128; pc += (int)(blockDim.x >> 5)) {
+      const int i = (pc & 1) * 32 + lane, j = ((pc >> 1) + lane) & 63;
+      dst[j * 64 + i] = src[i * 64 + j];
+    }
+    return;
+  }
   for (int idx = (int)threadIdx.x; idx < mp * mp; idx += (int)blockDim.x)
     dst[(idx % mp) * mp + idx / mp] = src[idx];
 }
@@ -234,9 +276,9 @@ struct NysLyCfg {
   // loads), not of 32 (the transposed writes spread over 8 banks)
   static constexpr int kLd = 68;
   // shared floats: R0 = qtT [D][kLd] (then W [64][D]), R1 = ktT [D][kLd],
-  // eight 64 x 64 matrices (A, At, M, Mt, X, Xt, T1, T2), red [128]
+  // eight 64 x 64 matrices (A, At, M, Mt, X, Xt, T1, T2), red [132]
   static constexpr int kR = D * kLd > 64 * D ? D * kLd : 64 * D;
-  static constexpr int kFloats = 2 * kR + 8 * 64 * 64 + 128;
+  static constexpr int kFloats = 2 * kR + 8 * 64 * 64 + 132;
   static constexpr int kSmemBytes = kFloats * 4;
   static_assert(kSmemBytes <= 227 * 1024, "more shared memory than one CTA may have");
 };
@@ -277,26 +319,44 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
     seg_inv[t] = 1.f / (float)(hi - lo);
   }
   __syncthreads();
-#pragma unroll 4
-  for (int idx = t; idx < D * mp; idx += 512) {
-    const int i = idx / D, d = idx % D;
-    float qv = 0.f, kv = 0.f;
-    if (i < m) {
-      qv = p.qt32[((size_t)bh * m + i) * D + d];
-      const int parts = seg_parts[i];
-      const float* pk = p.kpart + (((size_t)bhk * m + i) * P) * D + d;
-      float s0 = 0.f, s1 = 0.f;  // two chains; the unrolled loads go out together
-      int k = 0;
-#pragma unroll 4
-      for (; k + 1 < parts; k += 2) {
-        s0 += pk[(size_t)k * D];
-        s1 += pk[(size_t)(k + 1) * D];
+  {
+    // Thread t: column d = t % D of rows i0, i0 + di, ... (all its loads
+    // issued before the sums that need them: one round trip per partial).
+    constexpr int kU = D * 64 / 512, di = 512 / D;
+    const int d = t % D, i0 = t / D;
+    float qv[kU], s0[kU], s1[kU];
+    int np[kU];
+    int maxp = 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * di;
+      qv[u] = 0.f;
+      s0[u] = 0.f;
+      s1[u] = 0.f;
+      np[u] = 0;
+      if (i < m) {
+        qv[u] = p.qt32[((size_t)bh * m + i) * D + d];
+        np[u] = seg_parts[i];
+        maxp = max(maxp, np[u]);
       }
-      if (k < parts) s0 += pk[(size_t)k * D];
-      kv = (s0 + s1) * seg_inv[i];
     }
-    qtT[d * LD + i] = qv;
-    ktT[d * LD + i] = kv;
+    // two chains per entry (even and odd partials), added at the end
+    for (int k = 0; k < maxp; k += 2) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float* pk = p.kpart + (((size_t)bhk * m + i0 + u * di) * P + k) * D + d;
+        if (k < np[u]) s0[u] += pk[0];
+        if (k + 1 < np[u]) s1[u] += pk[D];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * di;
+      if (i < mp) {
+        qtT[d * LD + i] = qv[u];
+        ktT[d * LD + i] = i < m ? (s0[u] + s1[u]) * seg_inv[i] : 0.f;
+      }
+    }
   }
   for (int idx = t; idx < mp * mp; idx += 512) A[idx] = 0.f;
   __syncthreads();  // (also: red is free again)
@@ -313,12 +373,7 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
     auto st = [&](int i, int j, float v) {
       if (i < m && j < m) A[i * mp + j] = v * p.scale;
     };
-    switch (mp) {
-      case 16: mm_tiles<1, 1>(qtT, LD, ktT, LD, D, 16, 16, st); break;
-      case 32: mm_tiles<1, 2>(qtT, LD, ktT, LD, D, 32, 32, st); break;
-      case 48: mm_tiles<2, 3>(qtT, LD, ktT, LD, D, 48, 48, st); break;
-      default: mm_tiles<2, 4>(qtT, LD, ktT, LD, D, 64, 64, st); break;
-    }
+    mm_blocks(qtT, LD, ktT, LD, D, mp, mp, st);
   }
   __syncthreads();
   {
@@ -342,9 +397,16 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
   __syncthreads();
   smem_transpose(A, At, mp);
   // W (rows >= m zero) into the region Qt occupied
-#pragma unroll 4
-  for (int idx = t; idx < mp * D; idx += 512)
-    W[idx] = idx < m * D ? p.w[(size_t)bh * m * D + idx] : 0.f;
+  {
+    const float4* wsrc = reinterpret_cast<const float4*>(p.w + (size_t)bh * m * D);
+    float4* wdst = reinterpret_cast<float4*>(W);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 64 * D / 4 / 512; ++u) {  // 16-byte pieces, rows >= m zero
+      const int idx = t + u * 512;
+      if (idx < mp * D / 4) wdst[idx] = idx < m * D / 4 ? wsrc[idx] : z;
+    }
+  }
   __syncthreads();
 
   // Newton-Schulz on M = A^T A + lambda I (ridge) or on A itself.  With the
@@ -394,13 +456,7 @@ __global__ void __launch_bounds__(512, 1) nys_lmy_kernel(const NysParams p) {
   {
     uint16_t* y = p.y16 + (size_t)bh * 2 * mp * D;
     auto st = [&](int i, int j, float v) { split_bf16(v, y[i * D + j], y[(mp + i) * D + j]); };
-    constexpr int TC = D / 32;
-    switch (mp) {
-      case 16: mm_tiles<1, TC>(Pt, mp, W, D, mp, 16, D, st); break;
-      case 32: mm_tiles<2, TC>(Pt, mp, W, D, mp, 32, D, st); break;
-      case 48: mm_tiles<3, TC>(Pt, mp, W, D, mp, 48, D, st); break;
-      default: mm_tiles<4, TC>(Pt, mp, W, D, mp, 64, D, st); break;
-    }
+    mm_blocks(Pt, mp, W, D, mp, mp, D, st);
   }
 }
 
