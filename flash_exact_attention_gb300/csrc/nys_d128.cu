@@ -11,7 +11,7 @@ cudaError_t launch_nys_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
   cudaError_t e;
   nys_pool_kernel<D><<<dim3(p.pool_splits, p.m, BH), 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  nys_qt_kernel<D><<<dim3(128, BH), D, 0, stream>>>(p);
+  nys_qt_kernel<D><<<dim3(128 * D / 4 / kNysSmallThreads, BH), kNysSmallThreads, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(nys_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -21,7 +21,13 @@ cudaError_t launch_nys_d128(const CUtensorMap& tq, const CUtensorMap& tk, const 
                      stream>>>(tqt, tk, tv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  nys_merge_kernel<D><<<dim3(p.m, BH), 4 * D, 0, stream>>>(p);
+  // merge: one chunk group per thread for a few chunks, four for many
+  if (p.kv_chunks <= 4)
+    nys_merge_kernel<D, 1><<<dim3((p.m * D / 4 + kNysSmallThreads - 1) / kNysSmallThreads, BH),
+                             kNysSmallThreads, 0, stream>>>(p);
+  else
+    nys_merge_kernel<D, 4><<<dim3((p.m * D + kNysSmallThreads - 1) / kNysSmallThreads, BH),
+                             kNysSmallThreads, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(nys_lmy_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

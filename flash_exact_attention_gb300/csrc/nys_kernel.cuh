@@ -107,29 +107,49 @@ __global__ void __launch_bounds__(256) nys_pool_kernel(const NysParams p) {
 }
 
 // ============================================================ 2: Qt
-// grid (128, B*Hq), D threads: row i of Qt (the mean of segment i: fp32 copy
-// and bf16 hi/lo pair in two 128-row tiles; rows >= m zero), column d per
-// thread, the split partial sums added in order.
+// grid (128 D / 4 / 256, B*Hq), 256 threads: thread (i, g) of head bh takes
+// row i of Qt, columns 4g .. 4g + 3 (the mean of segment i: fp32 copy and
+// bf16 hi/lo pair in two 128-row tiles; rows >= m zero), the split partial
+// sums added in order, two chains (even and odd splits) per column.
+constexpr int kNysSmallThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(D) nys_qt_kernel(const NysParams p) {
-  const int i = (int)blockIdx.x, bh = (int)blockIdx.y, d = (int)threadIdx.x;
+__global__ void __launch_bounds__(kNysSmallThreads) nys_qt_kernel(const NysParams p) {
+  constexpr int G = D / 4;
+  const int idx = (int)blockIdx.x * kNysSmallThreads + (int)threadIdx.x;
+  const int i = idx / G, d0 = (idx % G) * 4, bh = (int)blockIdx.y;
+  if (i >= 128) return;
   const int m = p.m, S = p.pool_splits;
-  float x = 0.f;
+  float x[4] = {0.f, 0.f, 0.f, 0.f};
   if (i < m) {
-    const float* pq = p.pool_part + ((size_t)bh * m + i) * S * D + d;
-    float s0 = 0.f, s1 = 0.f;  // two chains; the unrolled loads go out together
+    const float4* pq = reinterpret_cast<const float4*>(p.pool_part + ((size_t)bh * m + i) * S * D + d0);
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
     int k = 0;
 #pragma unroll 4
     for (; k + 1 < S; k += 2) {
-      s0 += pq[(size_t)k * D];
-      s1 += pq[(size_t)(k + 1) * D];
+      const float4 a = pq[(size_t)k * G], c = pq[(size_t)(k + 1) * G];
+      s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+      s1.x += c.x; s1.y += c.y; s1.z += c.z; s1.w += c.w;
     }
-    if (k < S) s0 += pq[(size_t)k * D];
-    x = (s0 + s1) / (float)(seg_lo(i + 1, p.N, m) - seg_lo(i, p.N, m));
-    p.qt32[((size_t)bh * m + i) * D + d] = x;
+    if (k < S) {
+      const float4 a = pq[(size_t)k * G];
+      s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+    }
+    const float len = (float)(seg_lo(i + 1, p.N, m) - seg_lo(i, p.N, m));
+    x[0] = (s0.x + s1.x) / len;
+    x[1] = (s0.y + s1.y) / len;
+    x[2] = (s0.z + s1.z) / len;
+    x[3] = (s0.w + s1.w) / len;
+    *reinterpret_cast<float4*>(p.qt32 + ((size_t)bh * m + i) * D + d0) =
+        make_float4(x[0], x[1], x[2], x[3]);
   }
-  uint16_t* q16 = p.qt16 + (size_t)bh * 2 * 128 * D + (size_t)i * D + d;
-  split_bf16(x, q16[0], q16[128 * D]);
+  uint16_t hi[4], lo[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) split_bf16(x[e], hi[e], lo[e]);
+  uint16_t* q16 = p.qt16 + (size_t)bh * 2 * 128 * D + (size_t)i * D + d0;
+  *reinterpret_cast<uint2*>(q16) = make_uint2(hi[0] | ((uint32_t)hi[1] << 16),
+                                              hi[2] | ((uint32_t)hi[3] << 16));
+  *reinterpret_cast<uint2*>(q16 + 128 * D) = make_uint2(lo[0] | ((uint32_t)lo[1] << 16),
+                                                        lo[2] | ((uint32_t)lo[3] << 16));
 }
 
 // ============================================================ 5: landmarks, pinv, Y
@@ -194,14 +214,15 @@ __device__ __forceinline__ void mm_blocks_t(const float* At, int lda, const floa
 }
 
 // The register tile for a shape: 8 x 4 for the 64 x 64 products over 64 steps
-// (4 warps; 12 wavefronts per 1024 multiply-adds), 4 x 4 where MR is a multiple
-// of 32, else 2 x 4.
+// (4 warps; 12 wavefronts per 1024 multiply-adds), 4 x 4 for the other
+// products of at least 64 x 64 entries with MR a multiple of 32, else 2 x 4
+// (the smaller products, where more warps matter more).
 template <class Store>
 __device__ __forceinline__ void mm_blocks(const float* At, int lda, const float* B, int ldb, int K,
                                           int MR, int NC, Store store) {
   if (MR == 64 && NC == 64 && K <= 64)
     mm_blocks_t<8>(At, lda, B, ldb, K, MR, NC, store);
-  else if (MR % 32 == 0)
+  else if (MR % 32 == 0 && MR * NC >= 64 * 64)
     mm_blocks_t<4>(At, lda, B, ldb, K, MR, NC, store);
   else
     mm_blocks_t<2>(At, lda, B, ldb, K, MR, NC, store);
@@ -821,39 +842,85 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ============================================================ 4: merge
-// grid (m, B*Hq), 4 D threads: landmark row i of head bh,
+// grid (m D / 4 / (256 / R), B*Hq), 256 threads = R chunk groups x 256 / R
+// (row, column quad) pairs: landmark row i of head bh, columns 4g .. 4g + 3,
 // W_i = sum_c 2^(mu_c - M) O_c / sum_c 2^(mu_c - M) l_c over the key chunks
-// (M the largest mu_c).  Thread (g, d) takes column d of chunks g, g+4, ...;
-// the four partial sums meet in shared memory.
-template <int D>
-__global__ void __launch_bounds__(4 * D) nys_merge_kernel(const NysParams p) {
-  __shared__ float part[4][D + 1];
-  __shared__ float den4[4];
-  __shared__ float mx4[4];
-  const int i = (int)blockIdx.x, bh = (int)blockIdx.y;
-  const int g = (int)threadIdx.x / D, d = (int)threadIdx.x % D;
+// (M the largest mu_c), each sum kept as four partial sums over the chunks
+// c = r mod 4 (r = 0..3) in order, added in that order at the end.  R = 1: one
+// thread keeps all four (few chunks); R = 4: group r keeps the r-th and the
+// four meet in shared memory (many chunks, four times the threads on them).
+template <int D, int R>
+__global__ void __launch_bounds__(kNysSmallThreads) nys_merge_kernel(const NysParams p) {
+  static_assert(R == 1 || R == 4, "one or four chunk groups");
+  constexpr int G = D / 4, PAIRS = kNysSmallThreads / R;
+  __shared__ float4 part[R == 4 ? 4 : 1][PAIRS];
+  __shared__ float dpart[R == 4 ? 4 : 1][PAIRS];
+  const int pr = (int)threadIdx.x % PAIRS, r = (int)threadIdx.x / PAIRS;
+  const int idx = (int)blockIdx.x * PAIRS + pr;
   const int m = p.m, C = p.kv_chunks;
-  const float* ml = p.kv_ml + ((size_t)bh * C * m + i) * 2;
-  const float* ob = p.kv_o + ((size_t)bh * C * m + i) * D + d;
+  const int i = idx / G, d0 = (idx % G) * 4, bh = (int)blockIdx.y;
+  const bool live = i < m;
+  const int il = live ? i : 0;
+  const float2* ml = reinterpret_cast<const float2*>(p.kv_ml) + (size_t)bh * C * m + il;
+  const float4* ob = reinterpret_cast<const float4*>(p.kv_o + ((size_t)bh * C * m + il) * D + d0);
+  const size_t ostep = (size_t)m * G;  // one chunk, in float4
+  __shared__ float mpart[R == 4 ? 4 : 1][PAIRS];
   float M = -INFINITY;
+  if constexpr (R == 1) {
 #pragma unroll 4
-  for (int c = g; c < C; c += 4) M = fmaxf(M, ml[(size_t)c * m * 2]);
-  if (d == 0) mx4[g] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-  float num = 0.f, den = 0.f;
+    for (int c = 0; c < C; ++c) M = fmaxf(M, ml[(size_t)c * m].x);
+  } else {  // each group the maximum over its chunks, then the four meet
 #pragma unroll 4
-  for (int c = g; c < C; c += 4) {
-    const float f = exp2f(ml[(size_t)c * m * 2] - M);
-    num = fmaf(f, ob[(size_t)c * m * D], num);
-    den = fmaf(f, ml[(size_t)c * m * 2 + 1], den);
+    for (int c = r; c < C; c += 4) M = fmaxf(M, ml[(size_t)c * m].x);
+    mpart[r][pr] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(mpart[0][pr], mpart[1][pr]), fmaxf(mpart[2][pr], mpart[3][pr]));
   }
-  part[g][d] = num;
-  if (d == 0) den4[g] = den;
-  __syncthreads();
-  if (g == 0)
-    p.w[((size_t)bh * m + i) * D + d] = (part[0][d] + part[1][d] + part[2][d] + part[3][d]) /
-                                        (den4[0] + den4[1] + den4[2] + den4[3]);
+  auto step = [&](int c, float4& nr, float& dr) {
+    const float2 v = ml[(size_t)c * m];
+    const float4 o = ob[(size_t)c * ostep];
+    const float f = exp2f(v.x - M);
+    nr.x = fmaf(f, o.x, nr.x);
+    nr.y = fmaf(f, o.y, nr.y);
+    nr.z = fmaf(f, o.z, nr.z);
+    nr.w = fmaf(f, o.w, nr.w);
+    dr = fmaf(f, v.y, dr);
+  };
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 n0 = z, n1 = z, n2 = z, n3 = z;
+  float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+  if constexpr (R == 1) {
+    int c = 0;
+    for (; c + 3 < C; c += 4) {
+      step(c, n0, e0);
+      step(c + 1, n1, e1);
+      step(c + 2, n2, e2);
+      step(c + 3, n3, e3);
+    }
+    if (c < C) step(c, n0, e0);
+    if (c + 1 < C) step(c + 1, n1, e1);
+    if (c + 2 < C) step(c + 2, n2, e2);
+  } else {
+#pragma unroll 4
+    for (int c = r; c < C; c += 4) step(c, n0, e0);
+    part[r][pr] = n0;
+    dpart[r][pr] = e0;
+    __syncthreads();
+    if (r != 0) return;
+    n0 = part[0][pr];
+    n1 = part[1][pr];
+    n2 = part[2][pr];
+    n3 = part[3][pr];
+    e0 = dpart[0][pr];
+    e1 = dpart[1][pr];
+    e2 = dpart[2][pr];
+    e3 = dpart[3][pr];
+  }
+  if (!live) return;
+  const float dn = e0 + e1 + e2 + e3;
+  *reinterpret_cast<float4*>(p.w + ((size_t)bh * m + i) * D + d0) =
+      make_float4((n0.x + n1.x + n2.x + n3.x) / dn, (n0.y + n1.y + n2.y + n3.y) / dn,
+                  (n0.z + n1.z + n2.z + n3.z) / dn, (n0.w + n1.w + n2.w + n3.w) / dn);
 }
 
 // ============================================================ 6: output pass
