@@ -176,11 +176,9 @@ def _ncu_kernel_key(name):
     return m.group(1), "%s<%s>" % (m.group(1), ",".join(args))
 
 
-def record_traffic(csv_path, workload, command):
-    """Reads an ncu --csv capture holding dram__bytes_read.sum and
-    dram__bytes_write.sum per launch, and records the median bytes per launch of
-    every kernel of the families above in profiles/dram_traffic.json, keyed by
-    (family, instantiation, workload) with the current source hash."""
+def _read_ncu_csv(csv_path):
+    """Launches of an ncu --csv capture: {launch id: {"name": kernel name,
+    metric: value}} for the DRAM byte counters (bytes) and the duration (us)."""
     import csv
     launches = {}
     with open(csv_path) as f:
@@ -196,41 +194,93 @@ def record_traffic(csv_path, workload, command):
                  "usecond": 1.0, "msecond": 1e3, "second": 1e6}.get(unit, 1.0)
         d = launches.setdefault(row["ID"], {"name": row["Kernel Name"]})
         d[mname] = d.get(mname, 0.0) + val * scale
-    per_kernel = {}
-    for d in launches.values():
-        fam, key = _ncu_kernel_key(d["name"])
-        if fam not in FAMILY_SOURCES or "dram__bytes_read.sum" not in d:
-            continue
-        per_kernel.setdefault((fam, key), []).append(d)
+    return launches
+
+
+def _launch_bytes(d):
+    return d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"]
+
+
+def _store_traffic_rows(recs):
+    """Adds the records to the traffic file, each replacing the row of the same
+    (family, kernel, workload)."""
     data = {"rows": []}
     if os.path.exists(TRAFFIC_JSON):
         with open(TRAFFIC_JSON) as f:
             data = json.load(f)
     rows = data.setdefault("rows", [])
-    for (fam, key), ds in sorted(per_kernel.items()):
-        wl = NEXT_ROW_KERNELS.get(key, workload)
-        nbytes = statistics.median(x["dram__bytes_read.sum"] + x["dram__bytes_write.sum"]
-                                   for x in ds)
-        rec = {"family": fam, "kernel": key, "workload": wl,
-               "source_hash": _kernel_source_hash(FAMILY_SOURCES[fam]),
-               "dram_bytes_per_launch": round(nbytes), "launches": len(ds),
-               "command": command}
-        if all("gpu__time_duration.sum" in x for x in ds):
-            rec["gpu_time_us_median_under_ncu"] = round(
-                statistics.median(x["gpu__time_duration.sum"] for x in ds), 2)
-        rows[:] = [r for r in rows if not (r.get("family") == fam and r.get("kernel") == key
-                                           and r.get("workload") == wl)]
+    for rec in recs:
+        rows[:] = [r for r in rows if not (r.get("family") == rec["family"]
+                                           and r.get("kernel") == rec["kernel"]
+                                           and r.get("workload") == rec["workload"])]
         rows.append(rec)
-        print("recorded %s on %s: %.0f bytes per launch (%d launches)" % (key, wl, nbytes,
-                                                                         len(ds)))
+        print("recorded %s on %s: %.0f bytes per launch" % (rec["kernel"], rec["workload"],
+                                                           rec["dram_bytes_per_launch"]))
     data["about"] = ("DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, "
                      "median over the captured launches) written by `python bench.py "
-                     "--record-traffic <ncu csv> --workload <name>`; bench.py uses a row "
-                     "only while the kernel family's source hash is unchanged")
+                     "--record-traffic <ncu csv> --workload <name>` (Nystrom: "
+                     "`--record-nystrom-traffic`, one call summed over its six kernels); "
+                     "bench.py uses a row only while the kernel family's source hash is "
+                     "unchanged")
     rows.sort(key=lambda r: (r["workload"], r["family"], r["kernel"]))
     with open(TRAFFIC_JSON, "w") as f:
         json.dump(data, f, indent=1)
         f.write("\n")
+
+
+def record_traffic(csv_path, workload, command):
+    """Reads an ncu --csv capture holding dram__bytes_read.sum and
+    dram__bytes_write.sum per launch, and records the median bytes per launch of
+    every kernel of the families above in profiles/dram_traffic.json, keyed by
+    (family, instantiation, workload) with the current source hash."""
+    per_kernel = {}
+    for d in _read_ncu_csv(csv_path).values():
+        fam, key = _ncu_kernel_key(d["name"])
+        if fam not in FAMILY_SOURCES or "dram__bytes_read.sum" not in d:
+            continue
+        per_kernel.setdefault((fam, key), []).append(d)
+    recs = []
+    for (fam, key), ds in sorted(per_kernel.items()):
+        rec = {"family": fam, "kernel": key, "workload": NEXT_ROW_KERNELS.get(key, workload),
+               "source_hash": _kernel_source_hash(FAMILY_SOURCES[fam]),
+               "dram_bytes_per_launch": round(statistics.median(_launch_bytes(x) for x in ds)),
+               "launches": len(ds), "command": command}
+        if all("gpu__time_duration.sum" in x for x in ds):
+            rec["gpu_time_us_median_under_ncu"] = round(
+                statistics.median(x["gpu__time_duration.sum"] for x in ds), 2)
+        recs.append(rec)
+    _store_traffic_rows(recs)
+
+
+# The Nystrom call's six kernels; the three streaming passes' traffic grows
+# with N, the other three (landmark algebra on m rows) do not.
+NYS_STREAMING = ("nys_pool_kernel", "nys_kv_kernel", "nys_out_kernel")
+NYS_KERNELS = NYS_STREAMING + ("nys_qt_kernel", "nys_merge_kernel", "nys_lmy_kernel")
+
+
+def record_nystrom_traffic(csv_path, workload, scale, command):
+    """DRAM bytes of one Nystrom call on `workload` from an ncu capture of the
+    same call at N / scale (a full-size call holds too much device memory for a
+    capture): per kernel the median bytes per launch, the streaming passes'
+    times `scale`, summed over the six kernels.  Recorded as the row
+    (nystrom_call, nystrom_call, workload)."""
+    per = {}
+    for d in _read_ncu_csv(csv_path).values():
+        fam = _ncu_kernel_key(d["name"])[0]
+        if fam in NYS_KERNELS and "dram__bytes_read.sum" in d:
+            per.setdefault(fam, []).append(_launch_bytes(d))
+    missing = [k for k in NYS_KERNELS if k not in per]
+    if missing:
+        raise SystemExit("capture lacks %s" % ", ".join(missing))
+    parts = {k: statistics.median(v) * (scale if k in NYS_STREAMING else 1)
+             for k, v in per.items()}
+    _store_traffic_rows([{
+        "family": "nystrom_call", "kernel": "nystrom_call", "workload": workload,
+        "source_hash": _kernel_source_hash(FAMILY_SOURCES["nystrom_call"]),
+        "dram_bytes_per_launch": round(sum(parts.values())), "launches": 1,
+        "per_kernel_bytes": {k: round(v) for k, v in sorted(parts.items())},
+        "captured_at": "N / %d, streaming passes scaled by %d" % (scale, scale),
+        "command": command}])
 
 
 class ClockSampler:
@@ -1053,16 +1103,23 @@ def main():
                     help="record the DRAM bytes per launch of an ncu --csv capture (metrics "
                          "dram__bytes_read.sum, dram__bytes_write.sum) taken on --workload "
                          "into profiles/dram_traffic.json, then exit")
+    ap.add_argument("--record-nystrom-traffic", nargs=3, metavar=("NCU_CSV", "ROW", "SCALE"),
+                    help="record one Nystrom call's DRAM bytes for the widened row ROW from "
+                         "an ncu --csv capture of the same call at N / SCALE, then exit")
     ap.add_argument("--record-command", default="",
                     help="the ncu command line the capture came from (stored beside it)")
     ap.add_argument("--traffic-json", default=None,
                     help="file the records go to (default profiles/dram_traffic.json)")
     args = ap.parse_args()
-    if args.record_traffic:
+    if args.record_traffic or args.record_nystrom_traffic:
         global TRAFFIC_JSON
         if args.traffic_json:
             TRAFFIC_JSON = args.traffic_json
-        record_traffic(args.record_traffic, args.workload, args.record_command)
+        if args.record_traffic:
+            record_traffic(args.record_traffic, args.workload, args.record_command)
+        else:
+            csv_path, row, scale = args.record_nystrom_traffic
+            record_nystrom_traffic(csv_path, row, int(scale), args.record_command)
         return
     if args.next_rows_only:
         groups = tuple(g for g in args.next_rows_only.split(",") if g)

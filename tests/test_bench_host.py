@@ -117,3 +117,38 @@ def test_clock_reader_parses_nvidia_smi_lines():
     when, sm, smax, active = c.samples[0]
     assert (sm, smax, active) == (2070.0, 2070.0, {"sw_power_cap"})
     assert when == datetime.datetime(2026, 12, 2, 10, 41, 0, 500000).timestamp()
+
+
+def test_record_nystrom_traffic_sums_one_call_and_scales_the_streaming_passes(tmp_path,
+                                                                               monkeypatch):
+    out = tmp_path / "dram_traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_JSON", str(out))
+    # (kernel, read MB, write MB): two calls, the second one's bytes 2 MB higher
+    kernels = [("void nys_pool_kernel<128>(NysParams)", 100.0, 1.0),
+               ("void nys_qt_kernel<128>(NysParams)", 2.0, 0.0),
+               ("void nys_kv_kernel<128>(CUtensorMap_st, NysParams)", 200.0, 5.0),
+               ("void nys_merge_kernel<128, 1>(NysParams)", 3.0, 0.0),
+               ("void nys_lmy_kernel<128>(NysParams)", 4.0, 0.0),
+               ("void nys_out_kernel<128>(CUtensorMap_st, NysParams)", 100.0, 100.0)]
+    rows, lid = [], 0
+    for extra in (0.0, 2.0):
+        for name, rd, wr in kernels:
+            rows += [(lid, name, "dram__bytes_read.sum", "Mbyte", "%.1f" % (rd + extra)),
+                     (lid, name, "dram__bytes_write.sum", "Mbyte", "%.1f" % wr)]
+            lid += 1
+    csv_path = tmp_path / "nys.csv"
+    csv_path.write_text(_csv(rows))
+    bench.record_nystrom_traffic(str(csv_path), "nystrom_b4_h16_n131072_d128_m64", 8, "ncu ...")
+    data = json.loads(out.read_text())
+    (r,) = data["rows"]
+    assert (r["family"], r["kernel"]) == ("nystrom_call", "nystrom_call")
+    # medians: pool 102, qt 3, kv 206, merge 4, lmy 5, out 201 MB; streaming x 8
+    assert r["per_kernel_bytes"]["nys_kv_kernel"] == 8 * 206_000_000
+    assert r["per_kernel_bytes"]["nys_lmy_kernel"] == 5_000_000
+    assert r["dram_bytes_per_launch"] == 8 * (102 + 206 + 201) * 10**6 + (3 + 4 + 5) * 10**6
+    assert bench._recorded_traffic("nystrom_call", "nystrom_b4_h16_n131072_d128_m64") == \
+        r["dram_bytes_per_launch"]
+    # a capture without one of the six kernels is refused
+    csv_path.write_text(_csv([x for x in rows if "lmy" not in x[1]]))
+    with pytest.raises(SystemExit):
+        bench.record_nystrom_traffic(str(csv_path), "nystrom_b4_h16_n131072_d128_m64", 8, "")
