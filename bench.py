@@ -190,8 +190,9 @@ def _read_ncu_csv(csv_path):
             continue
         unit = (row.get("Metric Unit") or "").strip().lower()
         val = float(row["Metric Value"].replace(",", ""))
-        scale = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "nsecond": 1e-3,
-                 "usecond": 1.0, "msecond": 1e3, "second": 1e6}.get(unit, 1.0)
+        scale = {"byte": 1, "b": 1, "kbyte": 1e3, "kb": 1e3, "mbyte": 1e6, "mb": 1e6,
+                 "gbyte": 1e9, "gb": 1e9, "nsecond": 1e-3, "ns": 1e-3, "usecond": 1.0,
+                 "us": 1.0, "msecond": 1e3, "ms": 1e3, "second": 1e6, "s": 1e6}.get(unit, 1.0)
         d = launches.setdefault(row["ID"], {"name": row["Kernel Name"]})
         d[mname] = d.get(mname, 0.0) + val * scale
     return launches

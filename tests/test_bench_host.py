@@ -44,7 +44,8 @@ def test_record_traffic_writes_json_that_the_bench_reads(tmp_path, monkeypatch):
                  (lid, fwd, "dram__bytes_write.sum", "Mbyte", "%.1f" % wr),
                  (lid, fwd, "gpu__time_duration.sum", "usecond", "700")]
     rows += [(9, stj, "dram__bytes_read.sum", "Gbyte", "1.5"),
-             (9, stj, "dram__bytes_write.sum", "byte", "1,000")]
+             (9, stj, "dram__bytes_write.sum", "byte", "1,000"),
+             (9, stj, "gpu__time_duration.sum", "ns", "3,021,504")]  # ncu's short unit form
     csv_path = tmp_path / "cap.csv"
     csv_path.write_text(_csv(rows))
     bench.record_traffic(str(csv_path), "dense_b2_h16_n8192_d128", "ncu ...")
@@ -56,6 +57,8 @@ def test_record_traffic_writes_json_that_the_bench_reads(tmp_path, monkeypatch):
     # a kernel only the Stieltjes row launches goes under that row's name
     assert by_wl[("stj_kernel", "stieltjes_b2_h16_n8192_d128_q4")][
         "dram_bytes_per_launch"] == 1_500_001_000
+    assert by_wl[("stj_kernel", "stieltjes_b2_h16_n8192_d128_q4")][
+        "gpu_time_us_median_under_ncu"] == 3021.5
     assert bench._recorded_traffic("fwd_kernel", "dense_b2_h16_n8192_d128") == 245e6
     assert bench._recorded_traffic("bwd_kernel", "dense_b2_h16_n8192_d128") is None
     # a record taken on other sources is ignored
