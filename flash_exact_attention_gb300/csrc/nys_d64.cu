@@ -11,7 +11,12 @@ cudaError_t launch_nys_d64(const CUtensorMap& tq, const CUtensorMap& tk, const C
   cudaError_t e;
   nys_pool_kernel<D><<<dim3(p.pool_splits, p.m, BH), 256, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  nys_qt_kernel<D><<<dim3(128 * D / 4 / kNysSmallThreads, BH), kNysSmallThreads, 0, stream>>>(p);
+  // Qt: four columns per thread for a few splits, one for many
+  if (p.pool_splits < 8)
+    nys_qt_kernel<D, 4><<<dim3(128 * D / 4 / kNysSmallThreads, BH), kNysSmallThreads, 0,
+                          stream>>>(p);
+  else
+    nys_qt_kernel<D, 1><<<dim3(128, BH), D, 0, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(nys_kv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,

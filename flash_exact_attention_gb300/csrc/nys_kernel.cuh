@@ -40,6 +40,7 @@
 // as in exact flash attention.
 #pragma once
 #include <cuda.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 #include "ptx.cuh"
 #include "kernels.h"
@@ -107,49 +108,66 @@ __global__ void __launch_bounds__(256) nys_pool_kernel(const NysParams p) {
 }
 
 // ============================================================ 2: Qt
-// grid (128 D / 4 / 256, B*Hq), 256 threads: thread (i, g) of head bh takes
-// row i of Qt, columns 4g .. 4g + 3 (the mean of segment i: fp32 copy and
-// bf16 hi/lo pair in two 128-row tiles; rows >= m zero), the split partial
-// sums added in order, two chains (even and odd splits) per column.
+// grid (128 D / W / T, B*Hq), T threads: thread (i, g) of head bh takes row i
+// of Qt, columns W g .. W g + W - 1 (the mean of segment i: fp32 copy and bf16
+// hi/lo pair in two 128-row tiles; rows >= m zero), the split partial sums
+// added in order, two chains (even and odd splits) per column.  W = 4 (16-byte
+// loads, T = 256) when there are few splits; W = 1 (T = D) when there are
+// many, where the longer chains of loads want more threads and more SMs.
 constexpr int kNysSmallThreads = 256;
-template <int D>
-__global__ void __launch_bounds__(kNysSmallThreads) nys_qt_kernel(const NysParams p) {
-  constexpr int G = D / 4;
-  const int idx = (int)blockIdx.x * kNysSmallThreads + (int)threadIdx.x;
-  const int i = idx / G, d0 = (idx % G) * 4, bh = (int)blockIdx.y;
+template <int D, int W>
+__global__ void __launch_bounds__(W == 4 ? kNysSmallThreads : D) nys_qt_kernel(const NysParams p) {
+  static_assert(W == 1 || W == 4, "one or four columns per thread");
+  using V = typename std::conditional<W == 4, float4, float>::type;
+  constexpr int G = D / W;
+  const int idx = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  const int i = idx / G, d0 = (idx % G) * W, bh = (int)blockIdx.y;
   if (i >= 128) return;
   const int m = p.m, S = p.pool_splits;
-  float x[4] = {0.f, 0.f, 0.f, 0.f};
+  auto add = [](V& acc, const V& a) {
+    if constexpr (W == 4) {
+      acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+    } else {
+      acc += a;
+    }
+  };
+  float x[W];
+#pragma unroll
+  for (int e = 0; e < W; ++e) x[e] = 0.f;
   if (i < m) {
-    const float4* pq = reinterpret_cast<const float4*>(p.pool_part + ((size_t)bh * m + i) * S * D + d0);
-    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    const V* pq = reinterpret_cast<const V*>(p.pool_part + ((size_t)bh * m + i) * S * D + d0);
+    V s0, s1;
+    memset(&s0, 0, sizeof(V));
+    memset(&s1, 0, sizeof(V));
     int k = 0;
 #pragma unroll 4
     for (; k + 1 < S; k += 2) {
-      const float4 a = pq[(size_t)k * G], c = pq[(size_t)(k + 1) * G];
-      s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
-      s1.x += c.x; s1.y += c.y; s1.z += c.z; s1.w += c.w;
+      const V a = pq[(size_t)k * G], c = pq[(size_t)(k + 1) * G];
+      add(s0, a);
+      add(s1, c);
     }
-    if (k < S) {
-      const float4 a = pq[(size_t)k * G];
-      s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
-    }
+    if (k < S) add(s0, pq[(size_t)k * G]);
     const float len = (float)(seg_lo(i + 1, p.N, m) - seg_lo(i, p.N, m));
-    x[0] = (s0.x + s1.x) / len;
-    x[1] = (s0.y + s1.y) / len;
-    x[2] = (s0.z + s1.z) / len;
-    x[3] = (s0.w + s1.w) / len;
-    *reinterpret_cast<float4*>(p.qt32 + ((size_t)bh * m + i) * D + d0) =
-        make_float4(x[0], x[1], x[2], x[3]);
-  }
-  uint16_t hi[4], lo[4];
+    const float* f0 = reinterpret_cast<const float*>(&s0);
+    const float* f1 = reinterpret_cast<const float*>(&s1);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) split_bf16(x[e], hi[e], lo[e]);
+    for (int e = 0; e < W; ++e) x[e] = (f0[e] + f1[e]) / len;
+    V xv;
+    memcpy(&xv, x, sizeof(V));
+    *reinterpret_cast<V*>(p.qt32 + ((size_t)bh * m + i) * D + d0) = xv;
+  }
   uint16_t* q16 = p.qt16 + (size_t)bh * 2 * 128 * D + (size_t)i * D + d0;
-  *reinterpret_cast<uint2*>(q16) = make_uint2(hi[0] | ((uint32_t)hi[1] << 16),
-                                              hi[2] | ((uint32_t)hi[3] << 16));
-  *reinterpret_cast<uint2*>(q16 + 128 * D) = make_uint2(lo[0] | ((uint32_t)lo[1] << 16),
-                                                        lo[2] | ((uint32_t)lo[3] << 16));
+  if constexpr (W == 4) {
+    uint16_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_bf16(x[e], hi[e], lo[e]);
+    *reinterpret_cast<uint2*>(q16) = make_uint2(hi[0] | ((uint32_t)hi[1] << 16),
+                                                hi[2] | ((uint32_t)hi[3] << 16));
+    *reinterpret_cast<uint2*>(q16 + 128 * D) = make_uint2(lo[0] | ((uint32_t)lo[1] << 16),
+                                                          lo[2] | ((uint32_t)lo[3] << 16));
+  } else {
+    split_bf16(x[0], q16[0], q16[128 * D]);
+  }
 }
 
 // ============================================================ 5: landmarks, pinv, Y
