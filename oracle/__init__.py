@@ -48,6 +48,9 @@ def bind(lib):
     lib.oracle_fwd_rows.restype = i
     lib.oracle_bwd.argtypes = [d, d, d, d, i, i, i, i, i, i, ctypes.c_double, d, d, d]
     lib.oracle_bwd.restype = i
+    lib.oracle_bwd_dq_rows.argtypes = [d, d, d, d, i, i, i, i, i, i, ctypes.c_double,
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, d]
+    lib.oracle_bwd_dq_rows.restype = i
     lib.oracle_stj_fwd_rows.argtypes = [d, d, d, i, i, i, i, i, i, ctypes.c_double, i, i,
                                         ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, d, d]
     lib.oracle_stj_fwd_rows.restype = i
@@ -130,6 +133,24 @@ def bwd(q, k, v, do, causal, scale):
     if rc != 0:
         raise ValueError("oracle_bwd rejected its arguments")
     return dq, dk, dv
+
+
+def bwd_dq_rows(q, k, v, do, causal, scale, rows):
+    """dQ of selected rows (flat ids (b*Hq + h)*N + i), each from its own row
+    of scores: the dQ of ``bwd`` without the N x N work of the whole backward.
+    Returns dq [len(rows), D] in fp64."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, N, D = q.shape
+    Hkv = k.shape[1]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    dq = np.empty((rows.size, D), dtype=np.float64)
+    rc = _load().oracle_bwd_dq_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, Hq, Hkv, N, D,
+                                    int(bool(causal)), float(scale),
+                                    rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                    rows.size, _ptr(dq))
+    if rc != 0:
+        raise ValueError("oracle_bwd_dq_rows rejected its arguments")
+    return dq
 
 
 def stj_fwd_rows(q, k, v, causal, scale, order, steps, rows=None):

@@ -213,6 +213,66 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
 }
 
 /*
+ * dQ of selected query rows (the dQ_i line of the backward above), for
+ * problems too large for the whole backward: per row i of head h, the allowed
+ * scores, P_i = softmax, O_i = sum_j P_ij v_j, Delta_i = dO_i . O_i,
+ * dS_ij = P_ij (dO_i . v_j - Delta_i) and dQ_i = scale sum_j dS_ij k_j.
+ * rows: flat ids (b*Hq + h)*N + i.  dq: [nrows, D].
+ */
+int oracle_bwd_dq_rows(const double* q, const double* k, const double* v, const double* dout,
+                       int B, int Hq, int Hkv, int N, int D, int causal, double scale,
+                       const int64_t* rows, int64_t nrows, double* dq) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || D <= 0 || Hq % Hkv || !rows) return -1;
+  const int64_t G = Hq / Hkv;
+  const int64_t total = (int64_t)B * Hq * N;
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+    double* oi = (double*)malloc(sizeof(double) * D);
+    const int have = s && oi;
+    if (!have) {
+#pragma omp atomic write
+      err = -1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+      if (!have) continue;
+      const int64_t id = rows[r];
+      if (id < 0 || id >= total) {
+#pragma omp atomic write
+        err = -1;
+        continue;
+      }
+      const int64_t i = id % N, bh = id / N, h = bh % Hq, b = bh / Hq, hk = h / G;
+      const double* qi = q + at4(b, h, i, 0, Hq, N, D);
+      const double* doi = dout + at4(b, h, i, 0, Hq, N, D);
+      const double* kh = k + at4(b, hk, 0, 0, Hkv, N, D);
+      const double* vh = v + at4(b, hk, 0, 0, Hkv, N, D);
+      double* dqi = dq + r * (int64_t)D;
+      const int64_t n = row_scores(qi, kh, N, D, i, causal, scale, s);
+      row_softmax(s, n);
+      for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+      for (int64_t j = 0; j < n; ++j)
+        for (int64_t d = 0; d < D; ++d) oi[d] += s[j] * vh[j * D + d];
+      double delta = 0.0;
+      for (int64_t d = 0; d < D; ++d) delta += doi[d] * oi[d];
+      for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
+      for (int64_t j = 0; j < n; ++j) {
+        const double* vj = vh + j * D;
+        double dp = 0.0;
+        for (int64_t d = 0; d < D; ++d) dp += doi[d] * vj[d];
+        const double ds = s[j] * (dp - delta);
+        for (int64_t d = 0; d < D; ++d) dqi[d] += scale * ds * kh[j * D + d];
+      }
+    }
+    free(s);
+    free(oi);
+  }
+  return err;
+}
+
+/*
  * Stieltjes attention forward, a second method on the same tiling.
  * FlashStieltjes page, "Why touch softmax": weights
  * p_j = (lambda - s_j)^-q with the pole lambda above the best score, placed so

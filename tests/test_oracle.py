@@ -58,6 +58,31 @@ def test_bwd_matches_brute_force(B, Hq, Hkv, N, D, causal, scale):
     np.testing.assert_allclose(dv.ravel(), bv, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,N,D,causal,scale", [
+    (1, 2, 1, 5, 4, True, 0.5),
+    (2, 2, 2, 6, 3, False, 0.37),
+    (1, 4, 2, 4, 3, True, 1.1),
+])
+def test_bwd_dq_rows_match_brute_force(B, Hq, Hkv, N, D, causal, scale):
+    """The row-wise dQ (for problems too large for the whole backward) against
+    the pure-Python brute force, every row and a shuffled subset."""
+    q = _rand((B, Hq, N, D), 14)
+    k = _rand((B, Hkv, N, D), 15)
+    v = _rand((B, Hkv, N, D), 16)
+    do = _rand((B, Hq, N, D), 17)
+    bq, _, _ = brute_bwd(q.ravel().tolist(), k.ravel().tolist(), v.ravel().tolist(),
+                         do.ravel().tolist(), B, Hq, Hkv, N, D, causal, scale)
+    bq = np.asarray(bq).reshape(-1, D)
+    rows = np.arange(B * Hq * N)
+    np.testing.assert_allclose(oracle.bwd_dq_rows(q, k, v, do, causal, scale, rows), bq,
+                               rtol=0, atol=1e-12)
+    some = np.random.default_rng(0).permutation(rows)[: max(1, rows.size // 3)]
+    np.testing.assert_allclose(oracle.bwd_dq_rows(q, k, v, do, causal, scale, some), bq[some],
+                               rtol=0, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.bwd_dq_rows(q, k, v, do, causal, scale, [B * Hq * N])
+
+
 # --------------------------------------------------------- printed worked example
 def _read_gap_table():
     rows = []
