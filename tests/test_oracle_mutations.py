@@ -30,6 +30,7 @@ PINS = [
     lambda: pins.test_bwd_central_finite_differences(False),
     lambda: pins.test_bwd_central_finite_differences(True),
     lambda: pins.test_bwd_invariants(True),
+    lambda: pins.test_bwd_dq_rows_match_brute_force(1, 4, 2, 4, 3, True, 1.1),
 ]
 
 # (name, text in the source, planted replacement)
@@ -47,6 +48,8 @@ MUTATIONS = [
      "dvp[j * D + d] += ds * doi[d];"),
     ("dQ uses v instead of k", "dqi[d] += scale * ds * kh[j * D + d];",
      "dqi[d] += scale * ds * vh[j * D + d];"),
+    ("row-wise dQ drops Delta", "const double ds = s[j] * (dp - delta);",
+     "const double ds = s[j] * dp;"),
 ]
 
 
